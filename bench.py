@@ -1,0 +1,517 @@
+"""Benchmark of the PLE n-gram row-id hash on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
+one batch: the per-token index build (ple_build_token_index) and the row-id
+hash of every layer (ple_row_ids), two launches, through the C ABI.  The
+workload is the large prefill: T=262144 tokens in 4 requests, ngram_size 4,
+4 heads per order (12 heads), 8 layers, int64 ids, 20% adversarial boundary
+runs.  Inputs are resident in HBM before the timed region; 64 distinct input
+sets rotate (256 MiB of inputs) and two output buffers alternate (201 MB of
+row ids written per step), so no step finds its inputs in the 126 MB L2.
+
+Also measured, as extra keys: the row-id kernel's own duration (CUDA events
+around it on its stream) against the HBM roofline, the end-to-end rate with
+host buffers (pinned H2D of ids / cu_seqlens / context, the two calls, D2H of
+all row ids), the decode B=1 device time per call (a CUDA graph of 300 calls,
+median of 7 replays), and the CPU oracle on the host cores.
+
+--impl reference times the CPU oracle (the only reference this path has) on
+bounded samples of the same workload.
+
+Under torchrun (--gpus N > 1) every rank hashes its own seeded batch (weak
+scaling, no collective on the data path); the step time is the max over
+ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "row-ids/sec and % HBM roofline at large prefill; device µs/call at decode B=1"
+UNIT = "row-ids/s"
+L2_BYTES = 126 * 2 ** 20
+ROTATE = 64
+KERNEL_SOURCES = ["ple_row_ids.cu", "ple_divmod.cuh", "ple_internal.h"]
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "row_ids_prefill_262144_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "layer_gram_embedding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def workload_config(batch: wl.Batch, extra=None):
+    cfg = {
+        "workload": (f"{batch.name}: T={batch.num_tokens} in {batch.num_requests} requests, "
+                     f"ngram_size={batch.ngram_size}, heads_per_ngram={batch.heads_per_ngram} "
+                     f"(H={batch.num_heads}), L={batch.num_layers} layers, "
+                     f"{batch.ids.dtype.name} ids, 20% boundary runs"),
+        "num_tokens": batch.num_tokens,
+        "num_requests": batch.num_requests,
+        "ngram_size": batch.ngram_size,
+        "heads_per_ngram": batch.heads_per_ngram,
+        "num_heads": batch.num_heads,
+        "num_layers": batch.num_layers,
+        "ids_dtype": batch.ids.dtype.name,
+        "row_ids_per_step": batch.row_ids_per_call,
+        "launches_per_step": 2,
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.monotonic()
+
+    def mark_off(self):
+        self.t_off = time.monotonic()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        window = [r for t, r in rows if self.t_on and self.t_off and self.t_on <= t <= self.t_off]
+        used = window if window else [r for _, r in rows]
+        sm = [float(r[1]) for r in used if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(used), "samples_in_timed_region": len(window)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling; no data-path collective)
+
+
+class Dist:
+    def __init__(self, backend: str | None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1 and backend:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a baseline
+
+
+def oracle_rate(batch: wl.Batch, budget_s: float):
+    """Row ids/s of the oracle (index + hash) on the host, single-threaded, on
+    contiguous token samples of the workload sized to about budget_s."""
+    import oracle
+
+    def run(b):
+        req, local = oracle.token_index(b.cu_seqlens, b.num_requests, b.num_tokens, b.is_decode)
+        oracle.row_ids(b.ids, req, local, b.ngram_context, b.layer_multipliers, b.vocab_sizes,
+                       b.offsets, b.ngram_size, b.heads_per_ngram, b.boundary_id)
+
+    probe = wl.slice_batch(batch, 0, min(8192, batch.num_tokens))
+    t = time.perf_counter()
+    run(probe)
+    dt = max(time.perf_counter() - t, 1e-6)
+    per_token = dt / probe.num_tokens
+    n = int(min(batch.num_tokens, max(1024, budget_s / per_token)))
+    sample = wl.slice_batch(batch, 0, n)
+    t = time.perf_counter()
+    run(sample)
+    dt = time.perf_counter() - t
+    return sample.row_ids_per_call / dt, sample, dt
+
+
+def reference_arm(args):
+    dist = Dist(None)
+    if dist.rank != 0:
+        return 0
+    batch = wl.prefill_262144()
+    # calibrate the sample so that warmup + steps fit in about two minutes
+    import oracle
+    oracle.build()
+    rate, _, _ = oracle_rate(batch, 0.5)
+    per_step_s = min(30.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+    n_tok = int(min(batch.num_tokens, max(256, per_step_s * rate / (batch.num_layers *
+                                                                       batch.num_heads))))
+    starts = [(i * 9973) % max(1, batch.num_tokens - n_tok + 1) for i in range(args.steps +
+                                                                             args.warmup)]
+
+    def step(i):
+        s = wl.slice_batch(batch, starts[i], starts[i] + n_tok)
+        req, local = oracle.token_index(s.cu_seqlens, s.num_requests, s.num_tokens, False)
+        t = time.perf_counter()
+        oracle.row_ids(s.ids, req, local, s.ngram_context, s.layer_multipliers, s.vocab_sizes,
+                       s.offsets, s.ngram_size, s.heads_per_ngram, s.boundary_id)
+        oracle.token_index(s.cu_seqlens, s.num_requests, s.num_tokens, False)
+        return time.perf_counter() - t, s.row_ids_per_call
+
+    for i in range(args.warmup):
+        step(i)
+    total_t, total_rows = 0.0, 0
+    for i in range(args.warmup, args.warmup + args.steps):
+        dt, rows = step(i)
+        total_t += dt
+        total_rows += rows
+    value = total_rows / total_t
+    sample = (f"{args.steps} contiguous samples of {n_tok} tokens of {batch.name} (carried "
+              f"context at each cut), index build + row ids per sample")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": workload_config(batch, {"reference": "CPU oracle (plain C, single thread), "
+                                                       "the only reference this path has",
+                                          "sample_tokens_per_step": n_tok}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample, "host_cores": os.cpu_count()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def our_arm(args):
+    import torch
+
+    import layer_gram_embedding_gb300 as ple
+    from layer_gram_embedding_gb300 import build as lib_build
+
+    dist = Dist("nccl")
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    lib_build.build()
+    lib = ple.lib()
+    stream = torch.cuda.current_stream(device)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    # ---- inputs, resident in HBM: ROTATE seeded batches sharing the model's parameters
+    base = wl.prefill_262144(replay=1000 * dist.rank)
+    batches = [base] + [wl.prefill_262144(replay=1000 * dist.rank + r) for r in range(1, ROTATE)]
+    T, B, N, hpn, L, H = (base.num_tokens, base.num_requests, base.ngram_size,
+                          base.heads_per_ngram, base.num_layers, base.num_heads)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    M, vocab, off = to_dev(base.layer_multipliers), to_dev(base.vocab_sizes), to_dev(base.offsets)
+    sets = []
+    for b in batches:
+        sets.append(dict(ids=to_dev(b.ids), ctx=to_dev(b.ngram_context), cu=to_dev(b.cu_seqlens),
+                         req=torch.empty(T, dtype=torch.int32, device=device),
+                         local=torch.empty(T, dtype=torch.int32, device=device)))
+    outs = [torch.empty((L, T, H), dtype=torch.int64, device=device) for _ in range(2)]
+    P = ctypes.c_void_p
+    idx_args, row_args = [], []
+    for k, s in enumerate(sets):
+        idx_args.append((P(s["cu"].data_ptr()), B, T, 0, P(s["req"].data_ptr()),
+                         P(s["local"].data_ptr()), sh))
+        row_args.append((P(s["ids"].data_ptr()), ple.PLE_I64, T, P(s["req"].data_ptr()),
+                         P(s["local"].data_ptr()), P(s["ctx"].data_ptr()), B, N - 1,
+                         P(M.data_ptr()), P(vocab.data_ptr()), P(off.data_ptr()), H, N, hpn, L,
+                         base.boundary_id, P(outs[k % 2].data_ptr()), sh))
+    f_idx, f_rows = lib.ple_build_token_index, lib.ple_row_ids
+
+    def step(i, ev0=None, ev1=None):
+        k = i % ROTATE
+        st = f_idx(*idx_args[k])
+        if ev0 is not None:
+            ev0.record(stream)
+        st |= f_rows(*row_args[k])
+        if ev1 is not None:
+            ev1.record(stream)
+        if st:
+            raise RuntimeError(f"library call failed: status {st}")
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(visible.split(",")[dist.local_rank].strip() if visible else
+                          str(dist.local_rank))
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+
+    # parity spot check of the timed configuration against a stored oracle run
+    # is done by the test suite; here only the kernel is timed.
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    clocks.mark_on()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, *k_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    clocks.mark_off()
+    dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = [a.elapsed_time(b) for a, b in k_ev]
+    total_ms = dist.max(total_ms, device)
+    clk = clocks.stop()
+
+    rows_per_step = base.row_ids_per_call
+    value = dist.world * rows_per_step * args.steps / (total_ms / 1e3)
+    kern_avg_ms = float(np.mean(kern_ms))
+    idb = base.ids.dtype.itemsize
+    kernel_bytes = T * (idb + 8 + 8 * L * H) + B * (N - 1) * idb + 8 * L * (N + 2 * H)
+    peaks, peak_kind = measured_peaks()
+    achieved = kernel_bytes / (kern_avg_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            prof = json.load(fh)
+        if prof.get("kernel_source_sha256_16") == kernel_source_hash():
+            traffic = prof.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "kernel": "ple row_ids_kernel", "algorithmic_bytes_per_launch": kernel_bytes,
+                "kernel_ms_avg": kern_avg_ms, "kernel_ms_median": float(np.median(kern_ms)),
+                "peak_kind": peak_kind}
+
+    # ---- end to end through the public Python API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, ple, torch, device, stream, batches[:4], M, vocab, off)
+
+    decode = None if args.no_decode else decode_latency(ple, torch, device)
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rate, sample, dt = oracle_rate(base, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"tokens [0, {sample.num_tokens}) of {base.name} (index + row ids, "
+                         f"{dt:.1f} s, one thread)", "host_cores": os.cpu_count()}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": workload_config(base, {
+            "l2": f"inputs rotate over {ROTATE} seeded sets ({ROTATE * (T * 16 + 64) >> 20} MiB) "
+                  f"and 2 output buffers ({L * T * H * 8 / 1e6:.0f} MB written per step); "
+                  "no step's data fits the 126 MB L2",
+            "parallelism": f"replicas x{dist.world} (weak scaling, no collective)"}),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "decode_b1": decode,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
+    """The same metric through ple_build_token_index / ple_row_ids (the Python
+    binding) with host buffers: every step copies its ids, cu_seqlens and
+    context from pinned host memory, runs both calls, and copies every row id
+    back to pinned host memory."""
+    b0 = batches[0]
+    T, B, L, H = b0.num_tokens, b0.num_requests, b0.num_layers, b0.num_heads
+    host = []
+    for b in batches:
+        host.append(dict(ids=torch.from_numpy(b.ids).pin_memory(),
+                         cu=torch.from_numpy(b.cu_seqlens).pin_memory(),
+                         ctx=torch.from_numpy(np.ascontiguousarray(b.ngram_context)).pin_memory()))
+    d_ids = torch.empty(T, dtype=torch.int64, device=device)
+    d_cu = torch.empty(B + 1, dtype=torch.int32, device=device)
+    d_ctx = torch.empty((B, b0.ngram_size - 1), dtype=torch.int64, device=device)
+    req = torch.empty(T, dtype=torch.int32, device=device)
+    local = torch.empty(T, dtype=torch.int32, device=device)
+    out = torch.empty((L, T, H), dtype=torch.int64, device=device)
+    h_out = torch.empty((L, T, H), dtype=torch.int64).pin_memory()
+    steps = max(3, min(args.steps, 100))
+    h2d = T * 8 + (B + 1) * 4 + B * (b0.ngram_size - 1) * 8
+    d2h = L * T * H * 8
+
+    def step(i):
+        h = host[i % len(host)]
+        d_ids.copy_(h["ids"], non_blocking=True)
+        d_cu.copy_(h["cu"], non_blocking=True)
+        d_ctx.copy_(h["ctx"], non_blocking=True)
+        ple.ple_build_token_index(d_cu, B, T, False, req=req, local=local)
+        ple.ple_row_ids(d_ids, req, local, d_ctx, M, vocab, off, b0.ngram_size,
+                        b0.heads_per_ngram, b0.boundary_id, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1)
+    return {"value": b0.row_ids_per_call * steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+def decode_latency(ple, torch, device):
+    """Device µs per call of ple_row_ids at decode B=1: a CUDA graph of 300
+    back-to-back calls, median of 7 replays (the page's 7 x 300 method)."""
+    b = wl.decode(1)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    ids, ctx = to_dev(b.ids), to_dev(b.ngram_context)
+    M, vocab, off = to_dev(b.layer_multipliers), to_dev(b.vocab_sizes), to_dev(b.offsets)
+    req, local = ple.ple_build_token_index(None, 1, 1, True, device=device)
+    out = torch.empty((1, 1, 4), dtype=torch.int64, device=device)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    calls = 300
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
+    g.replay()
+    torch.cuda.synchronize(device)
+    per_call = []
+    for _ in range(7):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(device)
+        per_call.append(1e3 * e0.elapsed_time(e1) / calls)
+    return {"device_us_per_call": statistics.median(per_call), "launches_per_call": 1,
+            "method": "CUDA graph of 300 calls, median of 7 replays", "runs_us": per_call}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode B=1 latency")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of single-thread oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+    return our_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

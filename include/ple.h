@@ -1,0 +1,178 @@
+/*
+ * ple.h -- C ABI of the GB300 (sm_103a) PLE n-gram row-id hash library.
+ *
+ * The operation is the per-layer-embedding (PLE) n-gram row-id hash of
+ * FreeToken PR #338, "perf(ple): fuse the n-gram row-id hash into one Triton
+ * kernel" (section "What"): for every token of a ragged decode or prefill
+ * batch, find the token's n-gram window across its request's carried
+ * context, mark which shifts cross a boundary token, and hash each n-gram
+ * order with multiply / XOR into table row ids with a floored remainder plus
+ * a per-head offset.
+ *
+ * Conventions shared by every entry point:
+ *   - Every array argument is a DEVICE pointer (cudaMalloc'd or otherwise
+ *     device-accessible) owned by the caller.  The library allocates nothing,
+ *     keeps no per-call state, never reads device data on the host and never
+ *     synchronises.  Inputs are read-only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  All work is enqueued on it; the calls return before it runs.
+ *     The calls are safe to capture in a CUDA graph provided one call of the
+ *     same kind was made on the device before capture (the first call on a
+ *     device sets kernel attributes).
+ *   - Every argument check is done on the host from the scalar arguments and
+ *     pointer values only.  On any error nothing is launched and no output
+ *     is written.  A launch failure is reported as PLE_ERR_CUDA; the CUDA
+ *     error code is then available from ple_last_cuda_error().
+ *   - Pointers must be aligned to their element size (4 bytes for int32
+ *     arrays, 8 for int64 arrays); 16-byte alignment is not required.
+ *   - All integer arithmetic is int64 with two's-complement wrap-around, as
+ *     torch's int64 tensor ops do.
+ */
+#ifndef PLE_H_
+#define PLE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PLE_OK = 0,
+    PLE_ERR_NULL = 1,           /* a required pointer is NULL */
+    PLE_ERR_SIZE = 2,           /* a size or count is out of the supported range */
+    PLE_ERR_GEOMETRY_CTX = 3,   /* ctx_len != ngram_size - 1 */
+    PLE_ERR_GEOMETRY_HEADS = 4, /* num_heads != (ngram_size - 1) * heads_per_ngram */
+    PLE_ERR_DTYPE = 5,          /* id_dtype is neither PLE_I32 nor PLE_I64 */
+    PLE_ERR_ALIGN = 6,          /* a pointer is not aligned to its element size */
+    PLE_ERR_CUDA = 7            /* a CUDA call failed; see ple_last_cuda_error() */
+} ple_status;
+
+typedef enum { PLE_I32 = 0, PLE_I64 = 1 } ple_id_dtype;
+
+#define PLE_MAX_NGRAM 16   /* largest supported ngram_size */
+#define PLE_MAX_HEADS 256  /* largest supported heads per layer */
+
+/*
+ * ple_build_token_index -- per-token (request, offset) index.
+ *
+ * Defined by the second observation of section "What" (token t belongs to
+ * request req[t] at intra-request offset local[t]) and by the index note of
+ * section "Why it is safe" (a decode is one token per request at offset 0;
+ * a decode of B requests and a prefill of one B-token request have the same
+ * shape and opposite meaning).
+ *
+ *   cu_seqlens    [num_requests + 1] int32, device.  Request r owns tokens
+ *                 cu_seqlens[r] <= t < cu_seqlens[r+1].  Must be
+ *                 non-decreasing with cu_seqlens[0] = 0 and
+ *                 cu_seqlens[num_requests] = num_tokens (device data, not
+ *                 checked; other contents give unspecified but in-range
+ *                 req values).  Ignored (may be NULL) when is_decode != 0.
+ *   num_requests  B >= 1 when num_tokens > 0.  For a decode, B == num_tokens.
+ *   num_tokens    T, 0 <= T <= INT32_MAX.  T == 0 returns PLE_OK, no launch.
+ *   is_decode     non-zero: req[t] = t, local[t] = 0.
+ *                 zero: req[t] = r with cu_seqlens[r] <= t < cu_seqlens[r+1]
+ *                 (empty requests own no token), local[t] = t - cu_seqlens[r].
+ *   req, local    [T] int32 outputs, device.
+ *
+ * Errors: PLE_ERR_NULL, PLE_ERR_SIZE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ * One kernel launch.
+ */
+ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests,
+                                 int64_t num_tokens, int32_t is_decode, int32_t* req,
+                                 int32_t* local, void* stream);
+
+/*
+ * ple_row_ids -- the PLE n-gram row-id hash, all layers in one launch.
+ *
+ * Defined by section "What" of the page (packed window, boundary scan,
+ * per-n-gram multiply / XOR / remainder / offset; the boundary walk of the
+ * first observation and the window addressing of the second) and by section
+ * "Why it is safe" (torch.remainder's floored sign rule; the two geometry
+ * preconditions, raised rather than asserted).  With N = ngram_size,
+ * hpn = heads_per_ngram, H = (N-1)*hpn, C = N-1, p = C + local[t]:
+ *
+ *   W(t,s)  = input_ids[t-s]                        if local[t] >= s
+ *           = ngram_context[req[t]][C + local[t] - s] otherwise
+ *   shift s is valid iff no boundary id is among W(t,1..s) (the token itself
+ *   is not checked; s = 0 is always valid);
+ *   V(t,s)  = W(t,s) if shift s is valid, else boundary_id;
+ *   for n = 2..N and j < hpn, head h = (n-2)*hpn + j:
+ *     mix   = XOR over s < n of V(t,s) * layer_multipliers[l][s]   (wrapping)
+ *     out[l][t][h] = floormod(mix, vocab_sizes[l][h]) + offsets[l][h]
+ *   where floormod takes the divisor's sign (torch.remainder).
+ *
+ *   input_ids           [T] int32 or int64 (id_dtype), device.  int32 ids are
+ *                       sign-extended to int64.
+ *   id_dtype            PLE_I32 or PLE_I64; also the dtype of ngram_context.
+ *   num_tokens          T, 0 <= T <= INT32_MAX.  T == 0: PLE_OK, no launch.
+ *   req, local          [T] int32, device, e.g. from ple_build_token_index.
+ *                       Preconditions (device data, not checked): 0 <= req <
+ *                       B, and the tokens of a request are contiguous and in
+ *                       order, so 0 <= local[t] <= t.  Values outside these
+ *                       ranges are clamped into them: the kernel never reads
+ *                       out of bounds, but such rows are unspecified.
+ *   ngram_context       [B, ctx_len], dtype id_dtype, device: each request's
+ *                       last ctx_len ids before this batch, oldest first.
+ *   num_requests        B >= 1 when T > 0.
+ *   ctx_len             must equal N - 1 (else PLE_ERR_GEOMETRY_CTX).
+ *   layer_multipliers   [L, N] int64, device; M[l][s] multiplies the id s
+ *                       places left of the token (s = 0: the token).
+ *   vocab_sizes         [L, H] int64, device.  Any non-zero value; negative
+ *                       sizes follow torch.remainder (result in (v, 0]).  A
+ *                       zero size yields the head's offset (torch raises).
+ *   offsets             [L, H] int64, device.
+ *   num_heads           H; must equal (N-1)*hpn (else PLE_ERR_GEOMETRY_HEADS);
+ *                       at most PLE_MAX_HEADS.
+ *   ngram_size          N, 2 <= N <= PLE_MAX_NGRAM.
+ *   heads_per_ngram     hpn >= 1.
+ *   num_layers          L >= 1.  A per-layer call passes M + l*N,
+ *                       vocab_sizes + l*H, offsets + l*H and L = 1.
+ *   boundary_id         b, the boundary (eos) token id.
+ *   out                 [L, T, H] int64, device; every element is written.
+ *
+ * Errors: PLE_ERR_SIZE, PLE_ERR_GEOMETRY_CTX, PLE_ERR_GEOMETRY_HEADS (checked
+ * in that order, before anything else), then PLE_ERR_NULL, PLE_ERR_DTYPE,
+ * PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ * One kernel launch; no host reads; fixed grid for fixed (T, L, H, N).
+ */
+ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                       const int32_t* req, const int32_t* local, const void* ngram_context,
+                       int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
+                       const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
+                       int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
+                       int64_t boundary_id, int64_t* out, void* stream);
+
+/*
+ * ple_selftest_floor_mod -- diagnostic: the library's invariant-divisor
+ * floored remainder next to one computed with CUDA's own % operator.
+ *
+ * Section "Why it is safe" states that torch.remainder is floored while a
+ * plain % truncates, so the kernel fixes the sign explicitly.  The row-id
+ * kernel computes floormod(x, v) with a per-divisor reciprocal (Barrett
+ * reduction) instead of %; this entry point exposes that routine so tests
+ * can compare it, element by element, with CUDA's % plus the sign fix.
+ *
+ *   x, v        [n] int64, device (v may be anything; for v == 0 both
+ *               outputs are 0).
+ *   out_fast    [n] int64, device: the library's routine.
+ *   out_ref     [n] int64, device: CUDA's % followed by the sign fix.
+ *
+ * Errors: PLE_ERR_NULL, PLE_ERR_SIZE (n < 0), PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ */
+ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
+                                  int64_t* out_fast, int64_t* out_ref, void* stream);
+
+/* Static, NUL-terminated description of a status code ("unknown status"
+ * for values outside ple_status). */
+const char* ple_status_string(int32_t status);
+
+/* The CUDA error code (a cudaError_t value) behind the last PLE_ERR_CUDA
+ * returned on the calling thread, or 0. */
+int32_t ple_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLE_H_ */

@@ -1,0 +1,230 @@
+"""Thin Python binding of libple.so (argument marshalling only).
+
+Every function here checks and converts its arguments, then calls the C ABI
+entry point of the same name; all computation happens in the library's CUDA
+kernels on the tensors' device, on the current torch stream.  There is no CPU
+path: tensors that are not all on one CUDA device are refused with
+ValueError (FreeToken PR #338, "perf(ple): fuse the n-gram row-id hash into
+one Triton kernel", section "Why it is safe": the fused path runs only when
+every input is on the same CUDA device), and if the library is missing the
+first call raises RuntimeError.
+
+PyTorch is used only for device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PLE_OK = 0
+PLE_ERR_NULL = 1
+PLE_ERR_SIZE = 2
+PLE_ERR_GEOMETRY_CTX = 3
+PLE_ERR_GEOMETRY_HEADS = 4
+PLE_ERR_DTYPE = 5
+PLE_ERR_ALIGN = 6
+PLE_ERR_CUDA = 7
+PLE_I32 = 0
+PLE_I64 = 1
+PLE_MAX_NGRAM = 16
+PLE_MAX_HEADS = 256
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libple.so")
+
+# every symbol include/ple.h declares, with its ctypes signature
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+SIGNATURES = {
+    "ple_build_token_index": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
+    "ple_row_ids": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32,
+                           _I32, _I64, _P, _P]),
+    "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
+    "ple_status_string": (ctypes.c_char_p, [_I32]),
+    "ple_last_cuda_error": (_I32, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PleError(RuntimeError):
+    """A non-geometry failure reported by the library."""
+
+    def __init__(self, status: int, where: str):
+        msg = status_string(status)
+        if status == PLE_ERR_CUDA:
+            msg += f" (cudaError {lib().ple_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libple.so.  Raises RuntimeError if it was never built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"libple.so is not built ({LIB_PATH}); build it with "
+                        "layer_gram_embedding_gb300.build.build() -- there is no fallback path")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ple_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status == PLE_OK:
+        return
+    if status in (PLE_ERR_GEOMETRY_CTX, PLE_ERR_GEOMETRY_HEADS):
+        raise ValueError(f"{where}: {status_string(status)}")
+    raise PleError(status, where)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def _one_cuda_device(tensors, where: str) -> torch.device:
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError(f"{where}: every tensor must be on one CUDA device (got {sorted(map(str, devs))})")
+    return next(iter(devs))
+
+
+def _need(t: torch.Tensor, dtype, name: str, where: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{where}: {name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{where}: {name} must be contiguous")
+
+
+def ple_build_token_index(cu_seqlens, num_requests: int, num_tokens: int, is_decode: bool,
+                          req: torch.Tensor | None = None, local: torch.Tensor | None = None,
+                          device=None, stream=None):
+    """(req, local) int32 [T] for a decode (is_decode) or a cu_seqlens prefill.
+
+    cu_seqlens: int32 [num_requests + 1] CUDA tensor (ignored for a decode).
+    req / local: optional preallocated int32 [T] outputs (e.g. graph buffers).
+    """
+    where = "ple_build_token_index"
+    T = int(num_tokens)
+    tensors = [t for t in (cu_seqlens if not is_decode else None, req, local) if t is not None]
+    if device is None and not tensors:
+        raise ValueError(f"{where}: pass a device, cu_seqlens or the output buffers")
+    dev = torch.device(device) if device is not None else _one_cuda_device(tensors, where)
+    if tensors:
+        _one_cuda_device(tensors + [torch.empty(0, device=dev)], where)
+    if req is None:
+        req = torch.empty(T, dtype=torch.int32, device=dev)
+    if local is None:
+        local = torch.empty(T, dtype=torch.int32, device=dev)
+    for name, t in (("req", req), ("local", local)):
+        _need(t, torch.int32, name, where)
+        if t.numel() != T:
+            raise ValueError(f"{where}: {name} must have num_tokens elements")
+    cu_p = ctypes.c_void_p(0)
+    if not is_decode:
+        _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+        if cu_seqlens.numel() != int(num_requests) + 1:
+            raise ValueError(f"{where}: cu_seqlens must have num_requests + 1 elements")
+        cu_p = _ptr(cu_seqlens)
+    with torch.cuda.device(dev):
+        st = lib().ple_build_token_index(cu_p, int(num_requests), T, int(bool(is_decode)),
+                                         _ptr(req), _ptr(local), _stream_handle(stream, dev))
+    _check(st, where)
+    return req, local
+
+
+def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor, local: torch.Tensor,
+                ngram_context: torch.Tensor, layer_multipliers: torch.Tensor,
+                vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
+                heads_per_ngram: int, boundary_id: int, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Row ids [L, T, H] int64 (one launch for every layer).
+
+    input_ids [T] and ngram_context [B, ngram_size-1]: int32 or int64, same
+    dtype.  layer_multipliers [L, N] (or [N]), vocab_sizes and offsets
+    [L, H] (or [H]): int64.  out: optional fixed [L, T, H] int64 destination
+    (a graph replay then writes into a stable buffer).  ValueError on the two
+    geometry preconditions and on tensors not all on one CUDA device.
+    """
+    where = "ple_row_ids"
+    dev = _one_cuda_device([input_ids, req, local, ngram_context, layer_multipliers, vocab_sizes,
+                            offsets] + ([out] if out is not None else []), where)
+    if input_ids.dtype not in (torch.int32, torch.int64):
+        raise TypeError(f"{where}: input_ids must be int32 or int64")
+    if ngram_context.dtype != input_ids.dtype:
+        raise TypeError(f"{where}: ngram_context must have the dtype of input_ids")
+    if input_ids.dim() != 1:
+        raise ValueError(f"{where}: input_ids must be [T]")
+    T = input_ids.shape[0]
+    N = int(ngram_size)
+    M = layer_multipliers.reshape(1, -1) if layer_multipliers.dim() == 1 else layer_multipliers
+    vocab = vocab_sizes.reshape(1, -1) if vocab_sizes.dim() == 1 else vocab_sizes
+    off = offsets.reshape(1, -1) if offsets.dim() == 1 else offsets
+    L, H = vocab.shape[0], vocab.shape[1]
+    ctx = ngram_context
+    if ctx.dim() != 2:
+        raise ValueError(f"{where}: ngram_context must be [B, ctx_len]")
+    for name, t in (("input_ids", input_ids), ("ngram_context", ctx)):
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+    for name, t in (("req", req), ("local", local)):
+        _need(t, torch.int32, name, where)
+        if t.numel() != T:
+            raise ValueError(f"{where}: {name} must be [T]")
+    for name, t in (("layer_multipliers", M), ("vocab_sizes", vocab), ("offsets", off)):
+        _need(t, torch.int64, name, where)
+    if M.shape != (L, N):
+        raise ValueError(f"{where}: layer_multipliers must be [L, ngram_size]")
+    if off.shape != (L, H):
+        raise ValueError(f"{where}: offsets must have the shape of vocab_sizes")
+    if out is None:
+        out = torch.empty((L, T, H), dtype=torch.int64, device=dev)
+    else:
+        _need(out, torch.int64, "out", where)
+        if tuple(out.shape) not in ((L, T, H),) + (((T, H),) if L == 1 else ()):
+            raise ValueError(f"{where}: out must be [L, T, H]")
+    dtype_code = PLE_I64 if input_ids.dtype == torch.int64 else PLE_I32
+    with torch.cuda.device(dev):
+        st = lib().ple_row_ids(_ptr(input_ids), dtype_code, T, _ptr(req), _ptr(local), _ptr(ctx),
+                               ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
+                               int(heads_per_ngram), L, int(boundary_id), _ptr(out),
+                               _stream_handle(stream, dev))
+    _check(st, where)
+    return out
+
+
+def ple_selftest_floor_mod(x: torch.Tensor, v: torch.Tensor, stream=None):
+    """(library floored remainder, CUDA % with sign fix), elementwise."""
+    where = "ple_selftest_floor_mod"
+    dev = _one_cuda_device([x, v], where)
+    _need(x, torch.int64, "x", where)
+    _need(v, torch.int64, "v", where)
+    if x.shape != v.shape:
+        raise ValueError(f"{where}: x and v must have one shape")
+    fast = torch.empty_like(x)
+    ref = torch.empty_like(x)
+    with torch.cuda.device(dev):
+        st = lib().ple_selftest_floor_mod(_ptr(x), _ptr(v), x.numel(), _ptr(fast), _ptr(ref),
+                                          _stream_handle(stream, dev))
+    _check(st, where)
+    return fast, ref

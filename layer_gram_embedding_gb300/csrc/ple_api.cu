@@ -1,0 +1,166 @@
+// C ABI of the PLE n-gram row-id hash library (declared in include/ple.h).
+//
+// Every entry point validates its scalar arguments and pointer values on the
+// host, then enqueues exactly one kernel on the caller's stream.  Nothing is
+// allocated, nothing is read back, nothing is cached except per-device facts
+// (SM count, shared-memory limit) looked up once.
+#include <stdint.h>
+
+#include <mutex>
+
+#include "ple.h"
+#include "ple_internal.h"
+
+namespace ple {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_facts_mu;
+bool g_facts_ok[kMaxDevices];
+DeviceFacts g_facts[kMaxDevices];
+}  // namespace
+
+cudaError_t device_facts(DeviceFacts* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_facts_mu);
+    if (!g_facts_ok[dev]) {
+        DeviceFacts f;
+        e = cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&f.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        g_facts[dev] = f;
+        g_facts_ok[dev] = true;
+    }
+    *out = g_facts[dev];
+    return cudaSuccess;
+}
+
+}  // namespace ple
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+ple_status cuda_failure(cudaError_t e) {
+    g_last_cuda_error = (int32_t)e;
+    return PLE_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+extern "C" ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests,
+                                            int64_t num_tokens, int32_t is_decode, int32_t* req,
+                                            int32_t* local, void* stream) {
+    if (num_tokens < 0 || num_tokens > INT32_MAX) return PLE_ERR_SIZE;
+    if (num_tokens == 0) return PLE_OK;
+    if (num_requests < 1) return PLE_ERR_SIZE;
+    if (is_decode && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
+    if (!req || !local || (!is_decode && !cu_seqlens)) return PLE_ERR_NULL;
+    if (!aligned(req, 4) || !aligned(local, 4) || (!is_decode && !aligned(cu_seqlens, 4)))
+        return PLE_ERR_ALIGN;
+    (void)cudaGetLastError();  // start from a clean per-thread error state
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+    e = ple::launch_token_index(cu_seqlens, num_requests, num_tokens, is_decode, req, local, dev,
+                                static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
+}
+
+extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                                  const int32_t* req, const int32_t* local,
+                                  const void* ngram_context, int32_t num_requests,
+                                  int32_t ctx_len, const int64_t* layer_multipliers,
+                                  const int64_t* vocab_sizes, const int64_t* offsets,
+                                  int32_t num_heads, int32_t ngram_size, int32_t heads_per_ngram,
+                                  int32_t num_layers, int64_t boundary_id, int64_t* out,
+                                  void* stream) {
+    // sizes first, then the page's two geometry preconditions
+    if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
+        num_tokens < 0 || num_tokens > INT32_MAX)
+        return PLE_ERR_SIZE;
+    if (ctx_len != ngram_size - 1) return PLE_ERR_GEOMETRY_CTX;
+    if ((int64_t)num_heads != (int64_t)(ngram_size - 1) * heads_per_ngram)
+        return PLE_ERR_GEOMETRY_HEADS;
+    if (num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
+    if (num_tokens == 0) return PLE_OK;
+    if (num_requests < 1) return PLE_ERR_SIZE;
+    if (!input_ids || !req || !local || !ngram_context || !layer_multipliers || !vocab_sizes ||
+        !offsets || !out)
+        return PLE_ERR_NULL;
+    if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
+    const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
+    if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
+        !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
+        !aligned(offsets, 8) || !aligned(out, 8))
+        return PLE_ERR_ALIGN;
+
+    (void)cudaGetLastError();
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+
+    ple::RowIdsParams p;
+    p.ids = input_ids;
+    p.req = req;
+    p.local = local;
+    p.ctx = ngram_context;
+    p.mult = layer_multipliers;
+    p.vocab = vocab_sizes;
+    p.offsets = offsets;
+    p.out = out;
+    p.T = num_tokens;
+    p.boundary = boundary_id;
+    p.B = num_requests;
+    p.N = ngram_size;
+    p.hpn = heads_per_ngram;
+    p.H = num_heads;
+    p.L = num_layers;
+    p.ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
+    const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev);
+    if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
+    e = ple::launch_row_ids(p, id_bytes, cfg, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
+}
+
+extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
+                                             int64_t* out_fast, int64_t* out_ref, void* stream) {
+    if (n < 0) return PLE_ERR_SIZE;
+    if (n == 0) return PLE_OK;
+    if (!x || !v || !out_fast || !out_ref) return PLE_ERR_NULL;
+    if (!aligned(x, 8) || !aligned(v, 8) || !aligned(out_fast, 8) || !aligned(out_ref, 8))
+        return PLE_ERR_ALIGN;
+    (void)cudaGetLastError();
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+    e = ple::launch_selftest_floor_mod(x, v, n, out_fast, out_ref, dev,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
+}
+
+extern "C" const char* ple_status_string(int32_t status) {
+    switch (status) {
+        case PLE_OK: return "ok";
+        case PLE_ERR_NULL: return "a required pointer is NULL";
+        case PLE_ERR_SIZE: return "a size or count is out of the supported range";
+        case PLE_ERR_GEOMETRY_CTX: return "ngram_context must hold ngram_size - 1 ids per request";
+        case PLE_ERR_GEOMETRY_HEADS:
+            return "num_heads must equal (ngram_size - 1) * heads_per_ngram";
+        case PLE_ERR_DTYPE: return "id dtype must be PLE_I32 or PLE_I64";
+        case PLE_ERR_ALIGN: return "a pointer is not aligned to its element size";
+        case PLE_ERR_CUDA: return "a CUDA call failed";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int32_t ple_last_cuda_error(void) { return g_last_cuda_error; }

@@ -1,0 +1,67 @@
+// Internal launch interface between the C ABI (ple_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ple {
+
+// Tokens per warp tile of the row-id kernel (two per lane).
+constexpr int kTileTokens = 64;
+// Halo slots kept in front of each warp's staged ids (>= PLE_MAX_NGRAM - 1,
+// even so the tile itself starts 16-byte aligned).
+constexpr int kHaloSlots = 16;
+// Upper bound on warps per thread block of the row-id kernel.
+constexpr int kMaxWarps = 8;
+// Shared-memory budget for the per-head constants of one layer group.
+constexpr int kConstBudgetBytes = 48 * 1024;
+
+struct RowIdsParams {
+    const void* ids;        // [T] int32 or int64
+    const int32_t* req;     // [T]
+    const int32_t* local;   // [T]
+    const void* ctx;        // [B, N-1], dtype of ids
+    const int64_t* mult;    // [L, N]
+    const int64_t* vocab;   // [L, H]
+    const int64_t* offsets; // [L, H]
+    int64_t* out;           // [L, T, H]
+    int64_t T;
+    int64_t boundary;
+    int32_t B;
+    int32_t N;
+    int32_t hpn;
+    int32_t H;
+    int32_t L;
+    int32_t group_layers;   // layers handled per thread block (grid.y groups)
+    int32_t stage_pitch;    // odd row pitch (in int64) of the output staging tile
+    int32_t ids_vec_ok;     // ids pointer is 16-byte aligned
+};
+
+struct RowIdsLaunch {
+    dim3 grid;
+    dim3 block;
+    size_t smem_bytes;
+};
+
+// Per-device facts the launch configuration depends on, cached per device.
+struct DeviceFacts {
+    int sm_count;
+    int max_smem_optin;
+};
+
+cudaError_t device_facts(DeviceFacts* out);
+
+// Chooses grid/block/shared memory and fills p.group_layers / p.stage_pitch.
+RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev);
+cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                           cudaStream_t stream);
+
+cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
+                               int32_t* req, int32_t* local, const DeviceFacts& dev,
+                               cudaStream_t stream);
+
+cudaError_t launch_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
+                                      int64_t* out_fast, int64_t* out_ref, const DeviceFacts& dev,
+                                      cudaStream_t stream);
+
+}  // namespace ple

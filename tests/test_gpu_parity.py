@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA library against the CPU oracle, bit for bit.
+
+Every comparison is array equality: the hash is integer arithmetic, so the
+only acceptable difference is none (FreeToken PR #338, "perf(ple): fuse the
+n-gram row-id hash into one Triton kernel", section "Why it is safe": the
+fused kernel is byte-identical to the reference on prefill and decode shapes
+and after CUDA-graph replays).  Inputs come from the seeded generators in
+workloads.py; expected values come from the oracle only.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import layer_gram_embedding_gb300 as ple
+import oracle
+import workloads as wl
+from brute_force import brute_row_ids
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = torch.device("cuda:0")
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def oracle_index(batch):
+    return oracle.token_index(batch.cu_seqlens, batch.num_requests, batch.num_tokens,
+                              batch.is_decode)
+
+
+def oracle_rows(batch, req=None, local=None):
+    if req is None:
+        req, local = oracle_index(batch)
+    return oracle.row_ids(batch.ids, req, local, batch.ngram_context, batch.layer_multipliers,
+                          batch.vocab_sizes, batch.offsets, batch.ngram_size,
+                          batch.heads_per_ngram, batch.boundary_id)
+
+
+def gpu_index(batch):
+    cu = dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None
+    return ple.ple_build_token_index(cu, batch.num_requests, batch.num_tokens, batch.is_decode,
+                                     device=DEV)
+
+
+def gpu_rows(batch, ids=None, out=None):
+    req, local = gpu_index(batch)
+    return ple.ple_row_ids(dev(batch.ids) if ids is None else ids, req, local,
+                           dev(batch.ngram_context), dev(batch.layer_multipliers),
+                           dev(batch.vocab_sizes), dev(batch.offsets), batch.ngram_size,
+                           batch.heads_per_ngram, batch.boundary_id, out=out)
+
+
+def assert_same(got: torch.Tensor, expect: np.ndarray, what: str):
+    g = got.cpu().numpy()
+    assert g.shape == expect.shape, what
+    if not np.array_equal(g, expect):
+        bad = np.argwhere(g != expect)
+        raise AssertionError(f"{what}: {len(bad)} of {g.size} differ, first at {bad[0].tolist()}: "
+                             f"{g[tuple(bad[0])]} != {expect[tuple(bad[0])]}")
+
+
+WORKLOADS = {b.name + ("_i32" if b.ids.dtype == np.int32 else ""): b for b in wl.all_workloads()}
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_token_index_matches_oracle(name):
+    batch = WORKLOADS[name]
+    req, local = gpu_index(batch)
+    oreq, olocal = oracle_index(batch)
+    assert np.array_equal(req.cpu().numpy(), oreq)
+    assert np.array_equal(local.cpu().numpy(), olocal)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_row_ids_match_oracle_full_size(name):
+    """Every workload at its full size, in the launch configuration the
+    benchmark uses, compared element by element."""
+    batch = WORKLOADS[name]
+    assert_same(gpu_rows(batch), oracle_rows(batch), name)
+
+
+@pytest.mark.parametrize("chunk", range(6))
+def test_random_edge_batches(chunk):
+    """Small ragged batches spanning several 64-token tiles with ragged tails,
+    empty requests, decodes, ngram_size 2..8, heads 1..3 per order, 1..3
+    layers, boundary densities 0..1, INT64_MIN/MAX multipliers, and vocab
+    sizes at the 32-bit edges, negative, tiny and huge."""
+    for seed in range(chunk * 60, (chunk + 1) * 60):
+        dtype = np.int32 if seed % 3 == 0 else np.int64
+        batch = wl.random_batch(seed, T_max=200, ids_dtype=dtype)
+        assert_same(gpu_rows(batch), oracle_rows(batch), f"seed {seed}")
+
+
+@pytest.mark.parametrize("N", list(range(9, 17)))
+def test_long_ngrams_generic_path(N):
+    batch = wl.random_batch(5000 + N, N=N, hpn=2, L=2, T_max=150)
+    assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N}")
+
+
+@pytest.mark.parametrize("N,hpn", [(2, 1), (2, 255), (3, 128), (5, 64), (16, 17), (4, 85),
+                                   (3, 33), (9, 5)])
+def test_head_counts(N, hpn):
+    if (N - 1) * hpn > ple.PLE_MAX_HEADS:
+        pytest.skip("beyond PLE_MAX_HEADS")
+    batch = wl.random_batch(6000 + N * 1000 + hpn, N=N, hpn=hpn, L=2, T_max=100,
+                            vocab_mode="primes")
+    assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N} hpn={hpn}")
+
+
+def test_full_range_ids_and_extreme_boundary():
+    rng = np.random.default_rng(77)
+    for b in (wl.I64_MIN, wl.I64_MAX, 0, -1):
+        batch = wl.random_batch(int(rng.integers(0, 10 ** 6)), T_max=150, boundary=b)
+        ids = rng.integers(wl.I64_MIN, wl.I64_MAX, size=batch.num_tokens, dtype=np.int64,
+                           endpoint=True)
+        ids[rng.random(batch.num_tokens) < 0.2] = b
+        batch.ids = ids
+        assert_same(gpu_rows(batch), oracle_rows(batch), f"b={b}")
+
+
+@pytest.mark.parametrize("dtype", [np.int64, np.int32])
+def test_misaligned_ids_take_the_scalar_path(dtype):
+    """ids that are element-aligned but not 16-byte aligned."""
+    batch = wl.prefill_262144(ids_dtype=dtype)
+    batch = wl.Batch("mis", batch.ids[:70001], batch.ngram_context, None, False,
+                     batch.layer_multipliers, batch.vocab_sizes, batch.offsets, 4, 4)
+    batch.cu_seqlens = wl.cu_from_lengths([30000, 0, 40001, 0])
+    padded = torch.zeros(batch.num_tokens + 1, dtype=torch.from_numpy(batch.ids).dtype, device=DEV)
+    padded[1:] = dev(batch.ids)
+    ids = padded[1:]
+    assert ids.data_ptr() % 16 != 0
+    assert_same(gpu_rows(batch, ids=ids), oracle_rows(batch), "misaligned")
+
+
+def test_empty_batch():
+    batch = wl.prefill_512()
+    z = torch.empty(0, dtype=torch.int64, device=DEV)
+    zi = torch.empty(0, dtype=torch.int32, device=DEV)
+    out = ple.ple_row_ids(z, zi, zi, dev(batch.ngram_context), dev(batch.layer_multipliers),
+                          dev(batch.vocab_sizes), dev(batch.offsets), 3, 2, batch.boundary_id)
+    assert out.shape == (1, 0, 4)
+
+
+def test_per_layer_calls_with_row_pointers():
+    """A per-layer call passes the layer's rows of the parameter arrays and
+    L = 1 (invariant: a multi-layer call's slice l equals it)."""
+    batch = wl.mixed_8192()
+    full = gpu_rows(batch)
+    req, local = gpu_index(batch)
+    ids, ctx = dev(batch.ids), dev(batch.ngram_context)
+    M, vocab, off = dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets)
+    lib = ple.lib()
+    out = torch.empty((batch.num_tokens, batch.num_heads), dtype=torch.int64, device=DEV)
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    for l in (0, 17, 47):
+        st = lib.ple_row_ids(ids.data_ptr(), ple.PLE_I64, batch.num_tokens, req.data_ptr(),
+                             local.data_ptr(), ctx.data_ptr(), batch.num_requests, 4,
+                             M.data_ptr() + 8 * l * 5, vocab.data_ptr() + 8 * l * 32,
+                             off.data_ptr() + 8 * l * 32, 32, 5, 8, 1, batch.boundary_id,
+                             out.data_ptr(), stream)
+        assert st == ple.PLE_OK
+        assert torch.equal(out, full[l])
+
+
+@pytest.mark.parametrize("kind", ["decode_b1", "decode_b4", "decode_b8", "prefill_512"])
+def test_cuda_graph_capture_and_three_replays(kind):
+    """Capture the index build and the hash once on fixed buffers; replay
+    three times with fresh ids and context, each equal to the oracle."""
+    make = (lambda r: wl.decode(int(kind[-1]), r)) if kind.startswith("decode") else wl.prefill_512
+    b0 = make(0)
+    ids, ctx = dev(b0.ids), dev(b0.ngram_context)
+    M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
+    cu = dev(b0.cu_seqlens) if b0.cu_seqlens is not None else None
+    T, B = b0.num_tokens, b0.num_requests
+    req = torch.empty(T, dtype=torch.int32, device=DEV)
+    local = torch.empty(T, dtype=torch.int32, device=DEV)
+    out = torch.full((1, T, 4), -123, dtype=torch.int64, device=DEV)
+
+    def step():
+        ple.ple_build_token_index(cu, B, T, b0.is_decode, req=req, local=local, device=DEV)
+        ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, 3, 2, b0.boundary_id, out=out)
+
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        step()  # the documented call before capture
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    torch.cuda.synchronize(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for replay in (1, 2, 3):
+        fresh = make(replay)
+        nb = dataclasses.replace(b0, ids=fresh.ids, ngram_context=fresh.ngram_context)
+        ids.copy_(dev(nb.ids))
+        ctx.copy_(dev(nb.ngram_context))
+        g.replay()
+        torch.cuda.synchronize(DEV)
+        assert_same(out, oracle_rows(nb), f"{kind} replay {replay}")
+
+
+@pytest.mark.parametrize("what", ["ctx", "heads"])
+def test_refuses_a_geometry_it_cannot_address(what):
+    """ValueError, nothing launched, out untouched (a canary is checked)."""
+    batch = wl.prefill_512()
+    req, local = gpu_index(batch)
+    out = torch.full((1, 512, 4), 0x5EED, dtype=torch.int64, device=DEV)
+    ctx = dev(batch.ngram_context)
+    hpn = 2
+    if what == "ctx":
+        ctx = torch.zeros((1, 3), dtype=torch.int64, device=DEV)
+    else:
+        hpn = 1
+    with pytest.raises(ValueError):
+        ple.ple_row_ids(dev(batch.ids), req, local, ctx, dev(batch.layer_multipliers),
+                        dev(batch.vocab_sizes), dev(batch.offsets), 3, hpn, batch.boundary_id,
+                        out=out)
+    torch.cuda.synchronize(DEV)
+    assert bool((out == 0x5EED).all())
+
+
+def test_out_of_range_index_data_is_clamped_not_read_out_of_bounds():
+    """req outside [0, B) and local outside [0, t] are device data the host
+    cannot check; the kernel clamps them (req into [0, B-1], local into
+    [0, t]) and stays in bounds.  The rows then follow the page's addressing
+    rule on the clamped values, which the brute force evaluates directly."""
+    batch = wl.random_batch(4242, N=4, hpn=2, L=1, T_max=100, decode_batch=False)
+    T, B = batch.num_tokens, batch.num_requests
+    oreq, olocal = oracle_index(batch)
+    rng = np.random.default_rng(9)
+    req = oreq.copy()
+    local = olocal.copy()
+    pick = rng.random(T) < 0.3
+    req[pick] = rng.choice([-7, B, B + 100, 2 ** 31 - 1], size=int(pick.sum()))
+    pick = rng.random(T) < 0.3
+    local[pick] = rng.choice([-3, 10 ** 6, 2 ** 31 - 1], size=int(pick.sum()))
+    out = ple.ple_row_ids(dev(batch.ids), dev(req), dev(local), dev(batch.ngram_context),
+                          dev(batch.layer_multipliers), dev(batch.vocab_sizes),
+                          dev(batch.offsets), 4, 2, batch.boundary_id)
+    creq = np.clip(req, 0, B - 1)
+    clocal = np.minimum(np.maximum(local, 0), np.arange(T))
+    exp = np.array(brute_row_ids(batch.ids, creq, clocal, batch.ngram_context,
+                                 batch.layer_multipliers, batch.vocab_sizes, batch.offsets, 4, 2,
+                                 batch.boundary_id), dtype=np.int64)
+    assert_same(out, exp, "clamped index")
+
+
+def test_floor_mod_routine_matches_cuda_remainder():
+    """The invariant-divisor floored remainder against CUDA's own % plus the
+    sign fix, and against Python's floored %, on edge values."""
+    xs = [0, 1, -1, 2, -2, 10, -10, wl.I64_MAX, wl.I64_MIN, wl.I64_MIN + 1, wl.I64_MAX - 1,
+          2 ** 31, -(2 ** 31), 2 ** 32 - 1, -(2 ** 32), 2 ** 62, -(2 ** 62), 3 * 2 ** 61]
+    vs = wl.EDGE_VOCABS + [0, 5, 6, 2 ** 31 - 2, 2 ** 33 + 1, 2 ** 63 - 25]
+    pairs = [(x, v) for x in xs for v in vs]
+    for v in vs:
+        if v not in (0,):
+            for k in (-3, -2, -1, 1, 2, 3):
+                for d in (-1, 0, 1):
+                    y = k * v + d
+                    if wl.I64_MIN <= y <= wl.I64_MAX:
+                        pairs.append((y, v))
+    rng = np.random.default_rng(1)
+    rx = rng.integers(wl.I64_MIN, wl.I64_MAX, size=200000, dtype=np.int64, endpoint=True)
+    rv = rng.integers(wl.I64_MIN, wl.I64_MAX, size=200000, dtype=np.int64, endpoint=True)
+    rv = rv >> rng.integers(0, 63, size=200000)
+    x = np.concatenate([np.array([p[0] for p in pairs], np.int64), rx])
+    v = np.concatenate([np.array([p[1] for p in pairs], np.int64), rv])
+    fast, ref = ple.ple_selftest_floor_mod(dev(x), dev(v))
+    fast, ref = fast.cpu().numpy(), ref.cpu().numpy()
+    assert np.array_equal(fast, ref)
+    expect = np.array([(int(a) % int(b)) if b != 0 else 0 for a, b in zip(x, v)], dtype=np.int64)
+    assert np.array_equal(fast, expect)
+
+
+def test_stream_argument_is_honoured():
+    batch = wl.ragged_16()
+    s = torch.cuda.Stream(DEV)
+    with torch.cuda.stream(s):
+        out = gpu_rows(batch)
+    s.synchronize()
+    assert_same(out, oracle_rows(batch), "side stream")

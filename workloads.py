@@ -298,3 +298,33 @@ def random_batch(seed: int, T_max: int = 64, N=None, hpn=None, L=None, density=N
     batch = Batch(f"random_{seed}", ids, ctx, cu, is_decode, M, vocab, off, N, hpn, b,
                   meta={"density": density})
     return batch.with_ids_dtype(ids_dtype) if ids_dtype != np.int64 else batch
+
+
+def slice_batch(batch: Batch, start: int, stop: int) -> Batch:
+    """The tokens [start, stop) of a prefill batch as a batch of their own.
+
+    A request cut at `start` continues with a carried context: the last N-1
+    ids of (its context followed by its tokens before `start`), which is the
+    state the page's ngram_context carries from one call to the next, so the
+    slice's row ids equal the corresponding rows of the whole batch.  Only
+    ids are moved here; nothing is hashed.
+    """
+    if batch.is_decode:
+        ids = batch.ids[start:stop]
+        return replace(batch, name=f"{batch.name}[{start}:{stop}]", ids=ids,
+                       ngram_context=batch.ngram_context[start:stop])
+    C = batch.ngram_size - 1
+    cu = batch.cu_seqlens.astype(np.int64)
+    r_first = int(np.searchsorted(cu, start, side="right") - 1)
+    r_last = int(np.searchsorted(cu, max(stop - 1, start), side="right") - 1)
+    lengths, ctx_rows = [], []
+    for r in range(r_first, r_last + 1):
+        a, b = max(int(cu[r]), start), min(int(cu[r + 1]), stop)
+        if a > b:
+            a = b
+        lengths.append(b - a)
+        hist = np.concatenate([batch.ngram_context[r], batch.ids[int(cu[r]):a]])
+        ctx_rows.append(hist[len(hist) - C:])
+    ctx = np.stack(ctx_rows).astype(batch.ngram_context.dtype)
+    return replace(batch, name=f"{batch.name}[{start}:{stop}]", ids=batch.ids[start:stop],
+                   ngram_context=ctx, cu_seqlens=cu_from_lengths(lengths))
