@@ -124,6 +124,7 @@ extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64
     p.H = num_heads;
     p.L = num_layers;
     p.ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
+    p.out_vec_ok = aligned(out, 16) ? 1 : 0;
     const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev);
     if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
     e = ple::launch_row_ids(p, id_bytes, cfg, static_cast<cudaStream_t>(stream));

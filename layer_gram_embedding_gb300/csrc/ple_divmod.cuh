@@ -16,17 +16,19 @@
 //   PLDI 1994).  With d >= 1 and m = floor((2^64 - 1) / d), for any a < 2^64
 //   the estimate q' = floor(a * m / 2^64) satisfies q - 1 <= q' <= q, where
 //   q = floor(a / d):  m >= 2^64/d - 1 gives a*m/2^64 > a/d - 1, and
-//   m <= (2^64-1)/d gives a*m/2^64 < a/d.  So r' = a - q'*d lies in [0, 2d)
-//   and one conditional subtraction yields a mod d.
+//   m <= (2^64-1)/d gives a*m/2^64 < a/d.  So r' = a - q'*d lies in [0, 2d).
 //
-//   When d <= 2^31, r' < 2^32, so r' equals the low 32 bits of a - q'*d and
-//   only the low 32 bits of q' are needed: bits 64..95 of the 128-bit
-//   product a*m, which take four 32-bit partial products and one carry.
+//   When d <= 2^29, every remainder estimate below fits 32 bits, so only the
+//   low 32 bits of q' are needed: bits 64..95 of the 128-bit product a*m.
 //
-// The sign rule on top: with r = |x| mod |v|,
-//   v > 0: floormod(x, v) = r            if x >= 0,  (r ? |v| - r : 0) if x < 0
-//   v < 0: floormod(x, v) = -floormod(-x, |v|), i.e. the same with the
-//          condition flipped and the result negated.
+// The sign without a branch on it: the signed mix x is read in offset binary,
+// u = x + 2^63 (flip the top bit), so u is an unsigned value in [0, 2^64) and
+//   floormod(x, d) = (u - 2^63) mod d = (u mod d + d - (2^63 mod d)) mod d.
+// With D = d - (2^63 mod d) in [1, d] precomputed per head, adding D and a
+// few conditional subtractions finish the floored remainder; each is
+// min(r, r - k) on unsigned values (r - k wraps above r when r < k).
+// A negative divisor follows from floormod(x, v) = r ? r - |v| : 0 with
+// r = floormod(x, |v|), since the floored result lies in (v, 0].
 #pragma once
 
 #include <stdint.h>
@@ -36,18 +38,19 @@ namespace ple {
 enum : uint32_t {
     kHeadNegative = 1u,  // vocab < 0
     kHeadZero = 2u,      // vocab == 0: the row is the offset
-    kHeadFast = 4u,      // 0 < |vocab| <= 2^31: 32-bit remainder path
+    kHeadFast = 4u,      // 0 < vocab <= 2^29: 32-bit remainder path
 };
 
-// One head's divisor constants, 32 bytes, laid out so the fast path's fields
-// come in one 16-byte shared-memory load.
-struct __align__(16) HeadConst {
-    uint32_t m_lo;   // low / high words of m = floor((2^64 - 1) / |v|)
-    uint32_t m_hi;
-    uint32_t v_lo;   // |v| when it fits 32 bits
-    uint32_t kind;   // kHead* flags
-    int64_t off;     // the head's row offset
-    uint64_t v_abs;  // |v| (2^63 for INT64_MIN)
+// One head's constants, kept structure-of-arrays in shared memory so the
+// fast path reads 16 bytes per head and the offset separately:
+//   fast  = {m_lo, m_hi, |v| low word, D low word}, m = floor((2^64-1)/|v|),
+//           D = |v| - (2^63 mod |v|)
+//   off   = the head's row offset
+//   ext   = {|v| high word, D high word, kHead* flags, 0}
+struct HeadConst {
+    uint4 fast;
+    int64_t off;
+    uint4 ext;
 };
 
 __host__ __device__ __forceinline__ HeadConst make_head_const(int64_t v, int64_t off) {
@@ -55,74 +58,71 @@ __host__ __device__ __forceinline__ HeadConst make_head_const(int64_t v, int64_t
     const uint64_t va = v < 0 ? 0ull - (uint64_t)v : (uint64_t)v;
     // One call of the compiler's own 64-bit division per divisor.
     const uint64_t m = va ? (~0ull) / va : 0ull;
+    uint64_t d = 0;
+    if (va) {
+        // 2^63 mod |v| by the same Barrett step: for a = 2^63 the estimate
+        // floor(a * m / 2^64) is m >> 1.
+        uint64_t r = (1ull << 63) - (m >> 1) * va;
+        if (r >= va) r -= va;
+        d = va - r;
+    }
     uint32_t kind = 0;
     if (v < 0) kind |= kHeadNegative;
     if (va == 0) kind |= kHeadZero;
-    if (va != 0 && va <= (1ull << 31)) kind |= kHeadFast;
-    c.m_lo = (uint32_t)m;
-    c.m_hi = (uint32_t)(m >> 32);
-    c.v_lo = (uint32_t)va;
-    c.kind = kind;
+    if (v > 0 && va <= (1ull << 29)) kind |= kHeadFast;
+    c.fast = make_uint4((uint32_t)m, (uint32_t)(m >> 32), (uint32_t)va, (uint32_t)d);
     c.off = off;
-    c.v_abs = va;
+    c.ext = make_uint4((uint32_t)(va >> 32), (uint32_t)(d >> 32), kind, 0u);
     return c;
 }
 
-// a mod d for d <= 2^31, a < 2^64 (Barrett, low word only).
-__device__ __forceinline__ uint32_t mod_small(uint64_t a, uint32_t d, uint32_t m0, uint32_t m1) {
-    const uint32_t a0 = (uint32_t)a;
-    const uint32_t a1 = (uint32_t)(a >> 32);
-    const uint64_t p01 = (uint64_t)a0 * m1;
-    const uint64_t p10 = (uint64_t)a1 * m0;
-    const uint64_t mid = (uint64_t)__umulhi(a0, m0) + (uint32_t)p01 + (uint32_t)p10;
-    const uint32_t q_lo = a1 * m1 + (uint32_t)(p01 >> 32) + (uint32_t)(p10 >> 32) +
-                          (uint32_t)(mid >> 32);
-    const uint32_t r = a0 - q_lo * d;
-    return r >= d ? r - d : r;
-}
-
-// a mod d for any d >= 1, a < 2^64 (Barrett, full width).
-__device__ __forceinline__ uint64_t mod_wide(uint64_t a, uint64_t d, uint64_t m) {
-    const uint64_t q = __umul64hi(a, m);
-    const uint64_t r = a - q * d;
-    return r >= d ? r - d : r;
-}
-
-// |x| as an unsigned value and its sign; shared by every head of one order.
-struct Magnitude {
-    uint64_t a;
-    bool neg;
+// The signed mix in offset binary, split into 32-bit words.
+struct OffsetBinary {
+    uint32_t lo;
+    uint32_t hi;
 };
 
-__device__ __forceinline__ Magnitude magnitude(int64_t x) {
-    Magnitude r;
-    r.neg = x < 0;
-    r.a = r.neg ? 0ull - (uint64_t)x : (uint64_t)x;
+__device__ __forceinline__ OffsetBinary offset_binary(uint64_t mix) {
+    OffsetBinary u;
+    u.lo = (uint32_t)mix;
+    u.hi = (uint32_t)(mix >> 32) ^ 0x80000000u;
+    return u;
+}
+
+// floormod(x, v) for 0 < v <= 2^29 from x's offset binary u, given
+// c = {m_lo, m_hi, v, D}.  The quotient estimate keeps only the three
+// partial products that reach bits 64..95 of u*m and drops the carry out of
+// bits 32..63 (at most 2), so it can fall 3 short of floor(u/v): the
+// remainder estimate lies in [0, 4v), plus D in [1, 5v) < 2^32, and three
+// conditional subtractions (2v, 2v, v) finish it.
+__device__ __forceinline__ uint32_t floormod_fast(OffsetBinary u, uint4 c) {
+    const uint32_t q = u.hi * c.y + __umulhi(u.lo, c.y) + __umulhi(u.hi, c.x);
+    uint32_t r = u.lo - q * c.z + c.w;  // in [1, 5v)
+    const uint32_t v2 = c.z << 1;
+    r = min(r, r - v2);
+    r = min(r, r - v2);
+    r = min(r, r - c.z);
     return r;
 }
 
-// floormod(x, v) + off for the common case 0 < v <= 2^31.
-__device__ __forceinline__ int64_t row_fast_positive(const Magnitude& x, uint32_t m0, uint32_t m1,
-                                                     uint32_t v, int64_t off) {
-    const uint32_t r = mod_small(x.a, v, m0, m1);
-    const uint32_t t = (x.neg && r != 0u) ? v - r : r;
-    return (int64_t)((uint64_t)off + (uint64_t)t);
+__device__ __forceinline__ int64_t row_fast(OffsetBinary u, uint4 c, int64_t off) {
+    return (int64_t)((uint64_t)off + floormod_fast(u, c));
 }
 
 // floormod(x, v) + off for any head.
-__device__ __forceinline__ int64_t row_general(const Magnitude& x, const HeadConst& c) {
-    uint64_t r;
-    if (c.kind & kHeadZero) {
-        r = 0;
-    } else if (c.kind & kHeadFast) {
-        r = mod_small(x.a, c.v_lo, c.m_lo, c.m_hi);
-    } else {
-        r = mod_wide(x.a, c.v_abs, ((uint64_t)c.m_hi << 32) | c.m_lo);
-    }
-    const bool vneg = (c.kind & kHeadNegative) != 0;
-    const uint64_t t = ((x.neg != vneg) && r != 0) ? c.v_abs - r : r;
-    const uint64_t res = vneg ? 0ull - t : t;
-    return (int64_t)(res + (uint64_t)c.off);
+__device__ __forceinline__ int64_t row_general(OffsetBinary u, uint4 c, int64_t off, uint4 ext) {
+    if (ext.z & kHeadZero) return off;
+    const uint64_t a = ((uint64_t)u.hi << 32) | u.lo;
+    const uint64_t m = ((uint64_t)c.y << 32) | c.x;
+    const uint64_t va = ((uint64_t)ext.x << 32) | c.z;
+    const uint64_t d = ((uint64_t)ext.y << 32) | c.w;
+    const uint64_t q = __umul64hi(a, m);
+    uint64_t r = a - q * va;  // [0, 2|v|)
+    if (r >= va) r -= va;     // u mod |v|
+    r += d;                   // [1, 2|v|), no wrap: at most 2^64 - 1
+    if (r >= va) r -= va;     // floormod(x, |v|)
+    if (ext.z & kHeadNegative) r = r ? r - va : 0;
+    return (int64_t)(r + (uint64_t)off);
 }
 
 }  // namespace ple

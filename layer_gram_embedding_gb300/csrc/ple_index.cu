@@ -5,9 +5,11 @@
 // addresses the carried context (FreeToken PR #338, "perf(ple): fuse the
 // n-gram row-id hash into one Triton kernel", section "What", second
 // observation; section "Why it is safe": a decode is one token per request
-// at offset 0).  One thread per token; a prefill token finds its request by
-// binary search over cu_seqlens (the last r with cu_seqlens[r] <= t, which
-// skips empty requests).  Writes are coalesced int32 stores.
+// at offset 0).  Four consecutive tokens per thread and one 16-byte store of
+// each output when the outputs are 16-byte aligned; a prefill thread finds
+// its first token's request by binary search over cu_seqlens (staged in
+// shared memory when it has at most 4096 entries) and walks forward for the
+// other three.
 #include <stdint.h>
 
 #include "ple_divmod.cuh"
@@ -17,31 +19,79 @@ namespace ple {
 namespace {
 
 constexpr int kIndexThreads = 256;
+constexpr int kTokPerThread = 4;     // one 16-byte store of req and of local
+constexpr int kCuStaged = 4096;      // cu_seqlens entries kept in shared memory
 
-__global__ void __launch_bounds__(kIndexThreads)
-token_index_decode_kernel(int64_t T, int32_t* __restrict__ req, int32_t* __restrict__ local) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
-        req[t] = (int32_t)t;
-        local[t] = 0;
+template <bool kVec>
+__device__ __forceinline__ void store4(int32_t* __restrict__ req, int32_t* __restrict__ local,
+                                       int64_t t, int64_t T, const int (&r)[4], const int (&l)[4]) {
+    if (kVec && t + 3 < T) {
+        *reinterpret_cast<int4*>(req + t) = make_int4(r[0], r[1], r[2], r[3]);
+        *reinterpret_cast<int4*>(local + t) = make_int4(l[0], l[1], l[2], l[3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (t + k < T) {
+                req[t + k] = r[k];
+                local[t + k] = l[k];
+            }
+        }
     }
 }
 
+template <bool kVec>
+__global__ void __launch_bounds__(kIndexThreads)
+token_index_decode_kernel(int64_t T, int32_t* __restrict__ req, int32_t* __restrict__ local) {
+    cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * kTokPerThread;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kTokPerThread; t < T;
+         t += stride) {
+        const int r[4] = {(int)t, (int)t + 1, (int)t + 2, (int)t + 3};
+        const int l[4] = {0, 0, 0, 0};
+        store4<kVec>(req, local, t, T, r, l);
+    }
+}
+
+// Request of token t: the last r in [0, B-1] with cu[r] <= t (empty requests
+// own no token); the following tokens of the same thread walk forward.
+template <bool kVec, bool kStaged>
 __global__ void __launch_bounds__(kIndexThreads)
 token_index_prefill_kernel(const int32_t* __restrict__ cu, int32_t B, int64_t T,
                            int32_t* __restrict__ req, int32_t* __restrict__ local) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
+    // programmatic dependent launch, both ways: let a dependent row-id launch
+    // become resident now (it waits for this grid before reading the index),
+    // and wait for the previous kernel in the stream (which may still be
+    // reading req / local) before touching memory
+    cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize();
+    __shared__ int32_t cu_s[kStaged ? kCuStaged : 1];
+    const int32_t* c = cu;
+    if (kStaged) {
+        for (int i = threadIdx.x; i <= B; i += blockDim.x) cu_s[i] = __ldg(cu + i);
+        __syncthreads();
+        c = cu_s;
+    }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * kTokPerThread;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kTokPerThread; t < T;
+         t += stride) {
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             const int mid = lo + ((hi - lo + 1) >> 1);
-            if ((int64_t)__ldg(cu + mid) <= t)
+            if ((int64_t)c[mid] <= t)
                 lo = mid;
             else
                 hi = mid - 1;
         }
-        req[t] = lo;
-        local[t] = (int32_t)(t - (int64_t)__ldg(cu + lo));
+        int r[4], l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t tk = t + k;
+            while (lo < B - 1 && (int64_t)c[lo + 1] <= tk) ++lo;
+            r[k] = lo;
+            l[k] = (int)(tk - (int64_t)c[lo]);
+        }
+        store4<kVec>(req, local, t, T, r, l);
     }
 }
 
@@ -53,9 +103,9 @@ selftest_floor_mod_kernel(const int64_t* __restrict__ x, const int64_t* __restri
         const int64_t xi = x[i], vi = v[i];
         // the library's routine, exactly as the row-id kernel runs it
         const HeadConst c = make_head_const(vi, 0);
-        const Magnitude m = magnitude(xi);
-        out_fast[i] = (c.kind == kHeadFast) ? row_fast_positive(m, c.m_lo, c.m_hi, c.v_lo, 0)
-                                            : row_general(m, c);
+        const OffsetBinary u = offset_binary((uint64_t)xi);
+        out_fast[i] = (c.ext.z == kHeadFast) ? row_fast(u, c.fast, 0)
+                                             : row_general(u, c.fast, 0, c.ext);
         // CUDA's truncating % with the floored sign fix
         int64_t r = 0;
         if (vi != 0 && vi != -1) {
@@ -76,14 +126,40 @@ unsigned grid_for(int64_t n, const DeviceFacts& dev) {
 
 }  // namespace
 
+// Launch with programmatic stream serialization (see the kernels).
+template <typename... Args>
+cudaError_t launch_pdl(void (*fn)(Args...), unsigned grid, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kIndexThreads);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, fn, args...);
+}
+
 cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                int32_t* req, int32_t* local, const DeviceFacts& dev,
                                cudaStream_t stream) {
-    const unsigned g = grid_for(T, dev);
-    if (is_decode)
-        token_index_decode_kernel<<<g, kIndexThreads, 0, stream>>>(T, req, local);
-    else
-        token_index_prefill_kernel<<<g, kIndexThreads, 0, stream>>>(cu, B, T, req, local);
+    const unsigned g = grid_for((T + kTokPerThread - 1) / kTokPerThread, dev);
+    const bool vec = ((uintptr_t)req % 16 == 0) && ((uintptr_t)local % 16 == 0);
+    const bool staged = (int64_t)B + 1 <= kCuStaged;
+    cudaError_t e;
+    if (is_decode) {
+        e = vec ? launch_pdl(token_index_decode_kernel<true>, g, stream, T, req, local)
+                : launch_pdl(token_index_decode_kernel<false>, g, stream, T, req, local);
+    } else if (vec) {
+        e = staged ? launch_pdl(token_index_prefill_kernel<true, true>, g, stream, cu, B, T, req, local)
+                   : launch_pdl(token_index_prefill_kernel<true, false>, g, stream, cu, B, T, req, local);
+    } else {
+        e = staged ? launch_pdl(token_index_prefill_kernel<false, true>, g, stream, cu, B, T, req, local)
+                   : launch_pdl(token_index_prefill_kernel<false, false>, g, stream, cu, B, T, req, local);
+    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

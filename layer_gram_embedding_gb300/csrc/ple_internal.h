@@ -12,7 +12,15 @@ constexpr int kTileTokens = 64;
 // even so the tile itself starts 16-byte aligned).
 constexpr int kHaloSlots = 16;
 // Upper bound on warps per thread block of the row-id kernel.
-constexpr int kMaxWarps = 8;
+#ifndef PLE_MAX_WARPS
+#define PLE_MAX_WARPS 4
+#endif
+constexpr int kMaxWarps = PLE_MAX_WARPS;
+// Launch-shape target: thread blocks per SM the layer grouping aims for.
+#ifndef PLE_BLOCKS_PER_SM
+#define PLE_BLOCKS_PER_SM 16
+#endif
+constexpr int kTargetBlocksPerSm = PLE_BLOCKS_PER_SM;
 // Shared-memory budget for the per-head constants of one layer group.
 constexpr int kConstBudgetBytes = 48 * 1024;
 
@@ -33,8 +41,9 @@ struct RowIdsParams {
     int32_t H;
     int32_t L;
     int32_t group_layers;   // layers handled per thread block (grid.y groups)
-    int32_t stage_pitch;    // odd row pitch (in int64) of the output staging tile
+    int32_t stage_pitch;    // row pitch (in int64) of the output staging tile
     int32_t ids_vec_ok;     // ids pointer is 16-byte aligned
+    int32_t out_vec_ok;     // out pointer is 16-byte aligned
 };
 
 struct RowIdsLaunch {

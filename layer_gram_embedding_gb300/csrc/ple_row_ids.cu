@@ -15,17 +15,23 @@
 //
 // Work decomposition (one GPU, HBM-bound: 8*L*H bytes of row ids are written
 // per token against 16 bytes read):
-//   - grid.x covers the tokens in warp tiles of 64 (two per lane); grid.y
-//     splits the layers into groups so that even a small T fills the SMs.
+//   - grid.x covers the tokens in warp tiles of 64; grid.y splits the layers
+//     into groups so that even a small T fills the SMs.
 //   - Block prologue: the group's per-head divisor constants (one reciprocal
 //     per head, see ple_divmod.cuh) and multipliers go to shared memory.
 //   - Each warp stages its tile's ids plus an ngram_size-1 halo in shared
-//     memory (16-byte vector loads when aligned), then per 32-token half:
-//     builds V in registers with the carried boundary predicate, and per
-//     layer hashes every head into a shared staging tile whose odd row pitch
-//     makes the per-token writes bank-conflict free, then streams the tile
-//     out as contiguous, fully coalesced 8-byte stores ([L, T, H] layout:
-//     one warp-half covers 32*H consecutive int64).
+//     memory (16-byte vector loads when aligned) and builds each token's
+//     window V in registers with the carried boundary predicate.
+//   - Fixed shapes (the tuned (ngram_size, heads_per_ngram) pairs, even
+//     heads per order): each lane hashes two tokens per shared constant load,
+//     stages 32-bit remainders as head pairs in rows of odd pitch (8-byte
+//     stores hit 16 distinct bank pairs per half warp), and the readout walks
+//     the tile in global order ([L, T, H]), adds each head's offset in
+//     registers and stores 16 bytes per lane: a warp store covers 512
+//     consecutive bytes.
+//   - Any other shape: one token per lane, int64 rows staged with odd pitch,
+//     8-byte readout.  Heads off the 32-bit fast path (vocab outside
+//     (0, 2^29]) use the same int64 staging in either kernel.
 //   - No inter-warp communication after the prologue (warp-per-tile), no
 //     atomics, no host reads: the launch is graph-capturable.
 #include <stdint.h>
@@ -72,75 +78,79 @@ __device__ __forceinline__ void load_tile_vec<int32_t>(const int32_t* src, int64
     }
 }
 
-// Hash one layer for this lane's token into its staging row.
-template <int NMAX, int NT, bool kFast>
-__device__ __forceinline__ void hash_layer(const int64_t (&V)[NMAX], int N, int hpn,
-                                           const int64_t* __restrict__ ml,
-                                           const HeadConst* __restrict__ hl,
-                                           int64_t* __restrict__ srow) {
-    uint64_t mix = (uint64_t)V[0] * (uint64_t)ml[0];
-#pragma unroll
-    for (int s = 1; s < NMAX; ++s) {
-        if (NT == 0 && s >= N) break;
-        // order n = s + 1 folds shifts 0..s
-        mix ^= (uint64_t)V[s] * (uint64_t)ml[s];
-        const Magnitude x = magnitude((int64_t)mix);
-        const HeadConst* hs = hl + (s - 1) * hpn;
-        int64_t* so = srow + (s - 1) * hpn;
-#pragma unroll 4
-        for (int j = 0; j < hpn; ++j) {
-            if (kFast) {
-                const uint4 c = *reinterpret_cast<const uint4*>(hs + j);
-                so[j] = row_fast_positive(x, c.x, c.y, c.z, hs[j].off);
-            } else {
-                so[j] = row_general(x, hs[j]);
-            }
-        }
-    }
+// Per-block shared-memory layout, in order (all offsets 16-byte aligned):
+//   head constants of the layer group, structure of arrays:
+//     fast [G*H] uint4, off [G*H] int64 (padded to even), ext [G*H] uint4
+//   multipliers [G*N] int64 (padded to even)
+//   per warp: ids [kHaloSlots + kTileTokens] int64
+//   per warp: staging, stage_bytes(...) bytes
+struct SmemLayout {
+    uint4* fast;
+    int64_t* off;
+    uint4* ext;
+    int64_t* mul;
+    int64_t* ids;
+    unsigned char* stage;
+};
+
+__host__ __device__ constexpr size_t head_const_bytes(int heads) {
+    return (size_t)heads * 16 + (size_t)((heads + 1) & ~1) * 8 + (size_t)heads * 16;
 }
 
-template <typename IdT, int NT>
-__global__ void __launch_bounds__(kMaxWarps * 32)
-row_ids_kernel(const RowIdsParams p) {
-    constexpr int NMAX = NT > 0 ? NT : PLE_MAX_NGRAM;
-    const int N = NT > 0 ? NT : p.N;
-    const int H = p.H;
-    const int hpn = p.hpn;
-    const int pitch = p.stage_pitch;
-    const int G = p.group_layers;
-    const int l0 = blockIdx.y * G;
-    const int gl = min(G, p.L - l0);
-    const int nwarps = blockDim.x >> 5;
+// Staging bytes per warp.  Fixed shapes (even heads_per_ngram): 64 rows of
+// 32-bit remainders in 8-byte pairs, odd pitch (H/2 | 1) pairs, or 32 rows of
+// int64 rows with odd pitch (H | 1) for heads off the fast path -- whichever
+// is larger.  Runtime shapes: 32 rows of int64 with odd pitch.
+__host__ __device__ constexpr size_t stage_bytes(int H, bool fixed_shape) {
+    return fixed_shape ? ((size_t)64 * ((H / 2) | 1) * 8 > (size_t)32 * (H | 1) * 8
+                              ? (size_t)64 * ((H / 2) | 1) * 8
+                              : (size_t)32 * (H | 1) * 8)
+                       : (size_t)32 * (H | 1) * 8;
+}
 
-    extern __shared__ __align__(16) unsigned char smem[];
-    HeadConst* hc = reinterpret_cast<HeadConst*>(smem);
-    int64_t* mul_s = reinterpret_cast<int64_t*>(smem + (size_t)G * H * sizeof(HeadConst));
-    int64_t* ids_all = mul_s + ((G * N + 1) & ~1);
-    int64_t* stage_all = ids_all + nwarps * (kHaloSlots + kTileTokens);
+__device__ __forceinline__ SmemLayout carve_smem(unsigned char* base, int G, int H, int N,
+                                                 int nwarps) {
+    SmemLayout s;
+    const int gh = G * H;
+    s.fast = reinterpret_cast<uint4*>(base);
+    s.off = reinterpret_cast<int64_t*>(base + (size_t)gh * 16);
+    s.ext = reinterpret_cast<uint4*>(base + (size_t)gh * 16 + (size_t)((gh + 1) & ~1) * 8);
+    s.mul = reinterpret_cast<int64_t*>(base + head_const_bytes(gh));
+    s.ids = s.mul + ((G * N + 1) & ~1);
+    s.stage = reinterpret_cast<unsigned char*>(s.ids + nwarps * (kHaloSlots + kTileTokens));
+    return s;
+}
 
-    // ---- block prologue: this layer group's divisor constants and multipliers
+// Block prologue: the layer group's head constants and multipliers.
+// Returns this thread's vote on whether every head takes the 32-bit fast
+// path; the caller publishes the constants with __syncthreads_and once its
+// own window loads are in flight, so the per-head divisions overlap them.
+__device__ __forceinline__ int load_group_constants(const RowIdsParams& p, const SmemLayout& sm,
+                                                    int l0, int gl, int H, int N) {
     int fast = 1;
     for (int i = threadIdx.x; i < gl * H; i += blockDim.x) {
         const int64_t k = (int64_t)l0 * H + i;
         const HeadConst c = make_head_const(p.vocab[k], p.offsets[k]);
-        hc[i] = c;
-        fast &= (c.kind == kHeadFast) ? 1 : 0;
+        sm.fast[i] = c.fast;
+        sm.off[i] = c.off;
+        sm.ext[i] = c.ext;
+        fast &= (c.ext.z == kHeadFast) ? 1 : 0;
     }
-    for (int i = threadIdx.x; i < gl * N; i += blockDim.x) mul_s[i] = p.mult[(int64_t)l0 * N + i];
-    const bool all_fast = __syncthreads_and(fast) != 0;
+    for (int i = threadIdx.x; i < gl * N; i += blockDim.x) sm.mul[i] = p.mult[(int64_t)l0 * N + i];
+    return fast;
+}
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTileTokens;
-    if (t0 >= p.T) return;
-    const int ntile = (int)min((int64_t)kTileTokens, p.T - t0);
-    int64_t* ids_s = ids_all + warp * (kHaloSlots + kTileTokens) + kHaloSlots;
-    int64_t* stage = stage_all + (size_t)warp * 32 * pitch;
+// Programmatic dependent launch: the row-id kernel may be scheduled while
+// the kernel before it in the stream drains, so it waits for that grid's
+// completion (and memory) before its first global read.  Without the launch
+// attribute this returns at once.
+__device__ __forceinline__ void wait_prior_grid() { cudaGridDependencySynchronize(); }
+
+// Stage a warp tile's ids (and the N-1 ids left of it) in shared memory.
+template <typename IdT>
+__device__ __forceinline__ void stage_ids(const RowIdsParams& p, int64_t* ids_s, int64_t t0,
+                                          int ntile, int N, int lane) {
     const IdT* ids = static_cast<const IdT*>(p.ids);
-    const IdT* ctx = static_cast<const IdT*>(p.ctx);
-    const int64_t b = p.boundary;
-
-    // ---- stage the tile's ids and the N-1 ids left of it
     if (ntile == kTileTokens && p.ids_vec_ok) {
         load_tile_vec<IdT>(ids + t0, ids_s, lane);
     } else {
@@ -148,75 +158,307 @@ row_ids_kernel(const RowIdsParams p) {
     }
     if (lane < N - 1 && t0 - 1 - lane >= 0) ids_s[-1 - lane] = load_id<IdT>(ids, t0 - 1 - lane);
     __syncwarp();
+}
 
-    // staging readout walk: element e of a 32*H run sits at row e / H, column e % H
+// The shifted window V(t, 0..N-1) of tile token i with the carried boundary
+// predicate.  Index data outside the addressable ranges is clamped.
+template <typename IdT, int NMAX, int NT>
+__device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids_s, int64_t t0,
+                                       int i, bool live, int N, int64_t (&V)[NMAX]) {
+    const int64_t t = t0 + i;
+    int32_t r = 0, q = 0;
+    if (live) {
+        r = __ldg(p.req + t);
+        q = __ldg(p.local + t);
+    }
+    r = min(max(r, 0), p.B - 1);
+    q = (int32_t)min((int64_t)max(q, 0), t);
+    V[0] = live ? ids_s[i] : 0;
+    const IdT* crow = static_cast<const IdT*>(p.ctx) + (int64_t)r * (N - 1) + (N - 1) + q;
+    bool valid = true;
+#pragma unroll
+    for (int s = 1; s < NMAX; ++s) {
+        if (NT == 0 && s >= N) break;
+        const int64_t w = (q >= s) ? ids_s[i - s] : load_id<IdT>(crow, -s);
+        valid = valid && (w != p.boundary);
+        V[s] = valid ? w : p.boundary;
+    }
+}
+
+// Hash one layer for one token into its int64 staging row (8-byte stores).
+template <int NMAX, int NT, bool kFast>
+__device__ __forceinline__ void hash_layer(const int64_t (&V)[NMAX], int N, int hpn,
+                                           const int64_t* __restrict__ ml,
+                                           const uint4* __restrict__ hf,
+                                           const int64_t* __restrict__ ho,
+                                           const uint4* __restrict__ he,
+                                           int64_t* __restrict__ srow) {
+    uint64_t mix = (uint64_t)V[0] * (uint64_t)ml[0];
+#pragma unroll
+    for (int s = 1; s < NMAX; ++s) {
+        if (NT == 0 && s >= N) break;
+        // order n = s + 1 folds shifts 0..s
+        mix ^= (uint64_t)V[s] * (uint64_t)ml[s];
+        const OffsetBinary u = offset_binary(mix);
+        const int h0 = (s - 1) * hpn;
+#pragma unroll 4
+        for (int j = 0; j < hpn; ++j) {
+            const int h = h0 + j;
+            srow[h] = kFast ? row_fast(u, hf[h], ho[h]) : row_general(u, hf[h], ho[h], he[h]);
+        }
+    }
+}
+
+// Runtime-shape readout of one staged half tile (nsub tokens x H int64, row
+// pitch `pitch`): 8-byte units in global order, incremental (row, column).
+__device__ __forceinline__ void readout_runtime(const int64_t* __restrict__ stage,
+                                                long long* __restrict__ dst, int lane, int nsub,
+                                                int H, int pitch) {
     const int dq = 32 / H;
     const int dr = 32 % H;
-    const int q0 = lane / H;
-    const int r0 = lane % H;
+    int qq = lane / H;
+    int rr = lane % H;
+    const int nel = nsub * H;
+    for (int e = lane; e < nel; e += 32) {
+        __stcs(dst + e, (long long)stage[qq * pitch + rr]);
+        rr += dr;
+        qq += dq;
+        if (rr >= H) {
+            rr -= H;
+            ++qq;
+        }
+    }
+}
+
+// Any shape: one token per lane per half tile, int64 staging with odd pitch.
+template <typename IdT, int NT>
+__global__ void __launch_bounds__(kMaxWarps * 32)
+row_ids_kernel(const RowIdsParams p) {
+    constexpr int NMAX = NT > 0 ? NT : PLE_MAX_NGRAM;
+    const int N = NT > 0 ? NT : p.N;
+    const int H = p.H;
+    const int hpn = p.hpn;
+    const int pitch = H | 1;
+    const int G = p.group_layers;
+    const int l0 = blockIdx.y * G;
+    const int gl = min(G, p.L - l0);
+    const int nwarps = blockDim.x >> 5;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    wait_prior_grid();
+    const SmemLayout sm = carve_smem(smem, G, H, N, nwarps);
+    const int fast_vote = load_group_constants(p, sm, l0, gl, H, N);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTileTokens;
+    const int ntile = (int)max((int64_t)0, min((int64_t)kTileTokens, p.T - t0));
+    int64_t* ids_s = sm.ids + warp * (kHaloSlots + kTileTokens) + kHaloSlots;
+    int64_t* stage = reinterpret_cast<int64_t*>(sm.stage + (size_t)warp * stage_bytes(H, false));
+    if (ntile > 0) stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+    const bool all_fast = __syncthreads_and(fast_vote) != 0;
+    if (ntile == 0) return;
 
 #pragma unroll 1
     for (int u = 0; u < kTileTokens / 32; ++u) {
         const int nsub = min(32, ntile - 32 * u);
         if (nsub <= 0) break;
-        const int i = 32 * u + lane;
-        const int64_t t = t0 + i;
-        const bool live = lane < nsub;
-
-        // ---- the window and the carried boundary predicate
         int64_t V[NMAX];
-        {
-            int32_t r = 0, q = 0;
-            if (live) {
-                r = __ldg(p.req + t);
-                q = __ldg(p.local + t);
-            }
-            // keep device-side index data inside the ranges that can be addressed
-            r = min(max(r, 0), p.B - 1);
-            q = (int32_t)min((int64_t)max(q, 0), t);
-            V[0] = live ? ids_s[i] : 0;
-            const IdT* crow = ctx + (int64_t)r * (N - 1) + (N - 1) + q;
-            bool valid = true;
-#pragma unroll
-            for (int s = 1; s < NMAX; ++s) {
-                if (NT == 0 && s >= N) break;
-                const int64_t w = (q >= s) ? ids_s[i - s] : load_id<IdT>(crow, -s);
-                valid = valid && (w != b);
-                V[s] = valid ? w : b;
-            }
-        }
-
-        // ---- every layer of the group: hash into staging, stream out
+        window<IdT, NMAX, NT>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V);
 #pragma unroll 1
         for (int l = 0; l < gl; ++l) {
+            const int hb = l * H;
             if (all_fast)
-                hash_layer<NMAX, NT, true>(V, N, hpn, mul_s + l * N, hc + l * H, stage + lane * pitch);
+                hash_layer<NMAX, NT, true>(V, N, hpn, sm.mul + l * N, sm.fast + hb, sm.off + hb,
+                                           sm.ext + hb, stage + lane * pitch);
             else
-                hash_layer<NMAX, NT, false>(V, N, hpn, mul_s + l * N, hc + l * H, stage + lane * pitch);
+                hash_layer<NMAX, NT, false>(V, N, hpn, sm.mul + l * N, sm.fast + hb, sm.off + hb,
+                                            sm.ext + hb, stage + lane * pitch);
             __syncwarp();
             long long* dst = reinterpret_cast<long long*>(p.out) +
                              ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
-            const int nel = nsub * H;
-            int qq = q0, rr = r0;
-            for (int e = lane; e < nel; e += 32) {
-                __stcs(dst + e, (long long)stage[qq * pitch + rr]);
-                rr += dr;
-                qq += dq;
-                if (rr >= H) {
-                    rr -= H;
-                    ++qq;
-                }
-            }
+            readout_runtime(stage, dst, lane, nsub, H, pitch);
             __syncwarp();
         }
+    }
+}
+
+__host__ __device__ constexpr int gcd_const(int a, int b) { return b == 0 ? a : gcd_const(b, a % b); }
+
+// Fixed shapes with an even number of heads per order (the PLE
+// configurations this library is tuned for).  Each lane hashes two tokens of
+// the 64-token tile (lane and lane + 32) per constant load; the fast path
+// stages 32-bit remainders as pairs of heads, and the readout adds the head
+// offsets in registers and stores 16 bytes per lane in global order.
+template <int K, int P2, int NC, int GSTEP, bool kVec, bool kFull>
+__device__ __forceinline__ void readout_pairs(const uint2* __restrict__ st,
+                                              long long* __restrict__ dst, int lane, int nsub,
+                                              const int (&soff)[K], const int (&stok)[K],
+                                              const longlong2 (&offs)[NC]) {
+    longlong2* d2 = reinterpret_cast<longlong2*>(dst);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        if (kFull || stok[j] < nsub) {
+            const uint2 r = st[soff[j]];
+            const longlong2 o = offs[((32 * j) % K) / GSTEP];
+            const longlong2 rows = make_longlong2((long long)((unsigned long long)o.x + r.x),
+                                                  (long long)((unsigned long long)o.y + r.y));
+            if (kVec) {
+                __stcs(d2 + 32 * j + lane, rows);
+            } else {
+                long long* d1 = reinterpret_cast<long long*>(d2 + 32 * j + lane);
+                __stcs(d1, rows.x);
+                __stcs(d1 + 1, rows.y);
+            }
+        }
+    }
+}
+
+template <typename IdT, int NT, int HPT>
+__global__ void __launch_bounds__(kMaxWarps * 32)
+row_ids_fixed_kernel(const RowIdsParams p) {
+    static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
+    constexpr int N = NT;
+    constexpr int H = (NT - 1) * HPT;
+    constexpr int K = H / 2;        // 16-byte output chunks (head pairs) per token
+    constexpr int P2 = K | 1;       // staging row pitch in 8-byte pairs (odd)
+    constexpr int PG = H | 1;       // int64 staging pitch for the general path (odd)
+    constexpr int GSTEP = gcd_const(32, K);  // the steps (32 j) % K are its multiples
+    constexpr int NC = K / GSTEP;   // distinct readout columns per lane
+    static_assert(K <= 32, "readout walk assumes K <= 32");
+    const int G = p.group_layers;
+    const int l0 = blockIdx.y * G;
+    const int gl = min(G, p.L - l0);
+    const int nwarps = blockDim.x >> 5;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    wait_prior_grid();
+    const SmemLayout sm = carve_smem(smem, G, H, N, nwarps);
+    const int fast_vote = load_group_constants(p, sm, l0, gl, H, N);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTileTokens;
+    const int ntile = (int)max((int64_t)0, min((int64_t)kTileTokens, p.T - t0));
+    int64_t* ids_s = sm.ids + warp * (kHaloSlots + kTileTokens) + kHaloSlots;
+    unsigned char* stage = sm.stage + (size_t)warp * stage_bytes(H, true);
+    const int nA = min(32, ntile);
+    const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
+    int64_t VA[N], VB[N];
+    if (ntile > 0) {
+        stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+        window<IdT, N, N>(p, ids_s, t0, lane, lane < nA, N, VA);
+        window<IdT, N, N>(p, ids_s, t0, 32 + lane, lane < nB, N, VB);
+    }
+    const bool all_fast = __syncthreads_and(fast_vote) != 0;
+    if (ntile == 0) return;
+
+    if (!all_fast) {
+        // some head of this group is off the fast path: int64 rows, 8-byte
+        // readout, one half tile at a time
+        int64_t* st = reinterpret_cast<int64_t*>(stage);
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u) {
+            const int nsub = u == 0 ? nA : nB;
+            if (nsub <= 0) break;
+#pragma unroll 1
+            for (int l = 0; l < gl; ++l) {
+                const int hb = l * H;
+                hash_layer<N, N, false>(u == 0 ? VA : VB, N, HPT, sm.mul + l * N, sm.fast + hb,
+                                        sm.off + hb, sm.ext + hb, st + lane * PG);
+                __syncwarp();
+                long long* dst = reinterpret_cast<long long*>(p.out) +
+                                 ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
+                readout_runtime(st, dst, lane, nsub, H, PG);
+                __syncwarp();
+            }
+        }
+        return;
+    }
+
+    const uint2* stA = reinterpret_cast<const uint2*>(stage);
+    uint2* stAw = reinterpret_cast<uint2*>(stage);
+    // readout walk, the same for every layer: chunk c = 32 j + lane of a half
+    // tile is token c / K, column c % K; with q0 = lane / K, r0 = lane % K the
+    // step j adds the compile-time (32 j) / K and (32 j) % K, carrying one
+    // token when the column wraps
+    const int q0 = lane / K;
+    const int r0 = lane % K;
+    int soff[K], stok[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int cj = (32 * j) % K;
+        const bool carry = r0 + cj >= K;
+        stok[j] = q0 + (32 * j) / K + (carry ? 1 : 0);
+        soff[j] = stok[j] * P2 + r0 + cj - (carry ? K : 0);
+    }
+    const bool full = nA == 32 && nB == 32;
+    const bool vec_out = p.out_vec_ok != 0;
+
+#pragma unroll 1
+    for (int l = 0; l < gl; ++l) {
+        const int64_t* ml = sm.mul + l * N;
+        const uint4* hf = sm.fast + l * H;
+        uint64_t mixA = (uint64_t)VA[0] * (uint64_t)ml[0];
+        uint64_t mixB = (uint64_t)VB[0] * (uint64_t)ml[0];
+#pragma unroll
+        for (int s = 1; s < N; ++s) {
+            const uint64_t m = (uint64_t)ml[s];
+            mixA ^= (uint64_t)VA[s] * m;
+            mixB ^= (uint64_t)VB[s] * m;
+            const OffsetBinary uA = offset_binary(mixA);
+            const OffsetBinary uB = offset_binary(mixB);
+#pragma unroll
+            for (int j = 0; j < HPT; j += 2) {
+                const int h = (s - 1) * HPT + j;
+                const uint4 c0 = hf[h];
+                const uint4 c1 = hf[h + 1];
+                stAw[lane * P2 + h / 2] = make_uint2(floormod_fast(uA, c0), floormod_fast(uA, c1));
+                stAw[(32 + lane) * P2 + h / 2] =
+                    make_uint2(floormod_fast(uB, c0), floormod_fast(uB, c1));
+            }
+        }
+        // this lane's readout columns' offsets for layer l
+        longlong2 offs[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            int col = r0 + k * GSTEP;
+            col = col >= K ? col - K : col;
+            offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
+        }
+        __syncwarp();
+        long long* dst = reinterpret_cast<long long*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
+        if (full && vec_out) {
+            readout_pairs<K, P2, NC, GSTEP, true, true>(stA, dst, lane, 32, soff, stok, offs);
+            readout_pairs<K, P2, NC, GSTEP, true, true>(stA + 32 * P2, dst + 32 * H, lane, 32,
+                                                       soff, stok, offs);
+        } else if (vec_out) {
+            readout_pairs<K, P2, NC, GSTEP, true, false>(stA, dst, lane, nA, soff, stok, offs);
+            if (nB > 0)
+                readout_pairs<K, P2, NC, GSTEP, true, false>(stA + 32 * P2, dst + 32 * H, lane,
+                                                            nB, soff, stok, offs);
+        } else {
+            readout_pairs<K, P2, NC, GSTEP, false, false>(stA, dst, lane, nA, soff, stok, offs);
+            if (nB > 0)
+                readout_pairs<K, P2, NC, GSTEP, false, false>(stA + 32 * P2, dst + 32 * H, lane,
+                                                             nB, soff, stok, offs);
+        }
+        __syncwarp();
     }
 }
 
 template <typename IdT>
 using KernelFn = void (*)(const RowIdsParams);
 
+// Compile-time shapes: the PLE configurations this library is tuned for
+// (ngram_size, heads_per_ngram); everything else runs the runtime-shape
+// kernel for its ngram_size.
 template <typename IdT>
-KernelFn<IdT> pick_kernel(int N) {
+KernelFn<IdT> pick_kernel(int N, int hpn) {
+    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2>;
+    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4>;
+    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4>;
+    if (N == 5 && hpn == 8) return row_ids_fixed_kernel<IdT, 5, 8>;
     switch (N) {
         case 2: return row_ids_kernel<IdT, 2>;
         case 3: return row_ids_kernel<IdT, 3>;
@@ -229,9 +471,13 @@ KernelFn<IdT> pick_kernel(int N) {
     }
 }
 
+bool shape_is_fixed(int N, int hpn) {
+    return (N == 3 && (hpn == 2 || hpn == 4)) || (N == 4 && hpn == 4) || (N == 5 && hpn == 8);
+}
+
 template <typename IdT>
 cudaError_t launch_typed(const RowIdsParams& p, const RowIdsLaunch& cfg, cudaStream_t stream) {
-    const KernelFn<IdT> fn = pick_kernel<IdT>(p.N);
+    const KernelFn<IdT> fn = pick_kernel<IdT>(p.N, p.hpn);
     if (cfg.smem_bytes > 48 * 1024) {
         // Opting in to more than 48 KB of dynamic shared memory is a function
         // attribute; setting it is idempotent and not a stream operation.
@@ -239,7 +485,21 @@ cudaError_t launch_typed(const RowIdsParams& p, const RowIdsLaunch& cfg, cudaStr
                                              (int)cfg.smem_bytes);
         if (e != cudaSuccess) return e;
     }
-    fn<<<cfg.grid, cfg.block, cfg.smem_bytes, stream>>>(p);
+    // programmatic dependent launch: the blocks may become resident while the
+    // previous kernel in the stream (typically the token-index build) drains;
+    // the kernel waits for it before reading anything
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = cfg.grid;
+    lc.blockDim = cfg.block;
+    lc.dynamicSmemBytes = cfg.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&lc, fn, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -251,24 +511,26 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev) {
     RowIdsLaunch cfg;
     const int64_t tiles = (p.T + kTileTokens - 1) / kTileTokens;
     int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
+    const bool fixed_shape = shape_is_fixed(p.N, p.hpn);
     p.stage_pitch = p.H | 1;
-    const size_t per_warp = (size_t)(kHaloSlots + kTileTokens) * 8 + (size_t)32 * p.stage_pitch * 8;
+    const size_t per_warp =
+        (size_t)(kHaloSlots + kTileTokens) * 8 + stage_bytes(p.H, fixed_shape);
 
-    // layer groups: split the layers until there are ~8 blocks per SM, so the
-    // last wave is short even when T alone gives few tiles; constants stay
-    // within their shared-memory budget
+    // layer groups: split the layers until there are kTargetBlocksPerSm
+    // blocks per SM, so the last wave is short even when T alone gives few
+    // tiles; constants stay within their shared-memory budget
     int64_t blocks_x = (tiles + warps - 1) / warps;
-    const int64_t target = 8 * (int64_t)dev.sm_count;
+    const int64_t target = kTargetBlocksPerSm * (int64_t)dev.sm_count;
     int64_t groups = (target + blocks_x - 1) / blocks_x;
     if (groups < 1) groups = 1;
     if (groups > p.L) groups = p.L;
     int G = (int)((p.L + groups - 1) / groups);
-    const int g_cap = (int)(kConstBudgetBytes / ((size_t)p.H * sizeof(HeadConst)));
+    const int g_cap = (int)(kConstBudgetBytes / head_const_bytes(p.H));
     if (G > g_cap) G = g_cap > 0 ? g_cap : 1;
     groups = (p.L + G - 1) / G;
     p.group_layers = G;
 
-    const size_t fixed = (size_t)G * p.H * sizeof(HeadConst) + round_up((size_t)G * p.N, 2) * 8;
+    const size_t fixed = head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
     while (warps > 1 && fixed + warps * per_warp > (size_t)dev.max_smem_optin) --warps;
     blocks_x = (tiles + warps - 1) / warps;
     cfg.grid = dim3((unsigned)blocks_x, (unsigned)groups, 1);

@@ -77,6 +77,28 @@ def test_token_index_matches_oracle(name):
     assert np.array_equal(local.cpu().numpy(), olocal)
 
 
+@pytest.mark.parametrize("decode", [False, True])
+def test_token_index_paths(decode):
+    """Outputs that are 4- but not 16-byte aligned (scalar stores) and more
+    than 4096 requests (cu_seqlens read from global memory)."""
+    rng = np.random.default_rng(31)
+    B = 5000
+    lengths = np.ones(B, np.int64) if decode else rng.integers(0, 4, size=B)
+    T = int(lengths.sum())
+    cu = wl.cu_from_lengths(lengths)
+    oreq, olocal = oracle.token_index(None if decode else cu, B, T, decode)
+    buf = torch.full((2, T + 1), -9, dtype=torch.int32, device=DEV)
+    req, local = buf[0, 1:], buf[1, 1:]
+    assert req.data_ptr() % 16 != 0
+    ple.ple_build_token_index(None if decode else dev(cu), B, T, decode, req=req, local=local)
+    assert np.array_equal(req.cpu().numpy(), oreq)
+    assert np.array_equal(local.cpu().numpy(), olocal)
+    assert int(buf[0, 0]) == -9 and int(buf[1, 0]) == -9
+    req2, local2 = ple.ple_build_token_index(None if decode else dev(cu), B, T, decode, device=DEV)
+    assert np.array_equal(req2.cpu().numpy(), oreq)
+    assert np.array_equal(local2.cpu().numpy(), olocal)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_row_ids_match_oracle_full_size(name):
     """Every workload at its full size, in the launch configuration the
@@ -136,6 +158,19 @@ def test_misaligned_ids_take_the_scalar_path(dtype):
     ids = padded[1:]
     assert ids.data_ptr() % 16 != 0
     assert_same(gpu_rows(batch, ids=ids), oracle_rows(batch), "misaligned")
+
+
+@pytest.mark.parametrize("make", [wl.prefill_512, wl.ragged_16, wl.mixed_8192])
+def test_out_not_16_byte_aligned(make):
+    """out that is 8-byte but not 16-byte aligned takes the 8-byte readout."""
+    batch = make()
+    L, T, H = batch.num_layers, batch.num_tokens, batch.num_heads
+    buf = torch.full((L * T * H + 1,), -7, dtype=torch.int64, device=DEV)
+    out = buf[1:].view(L, T, H)
+    assert out.data_ptr() % 16 != 0
+    gpu_rows(batch, out=out)
+    assert int(buf[0]) == -7
+    assert_same(out, oracle_rows(batch), "misaligned out")
 
 
 def test_empty_batch():
