@@ -519,6 +519,79 @@ def decode_latency(ple, torch, device):
             "method": "CUDA graph of 300 calls, median of 7 replays", "runs_us": per_call}
 
 
+def all_configs(args):
+    """Every workload: device time per call of ple_row_ids and of a whole
+    step (index + row ids), each from a CUDA graph of 300 back-to-back calls,
+    median of 7 replays (the page's 7 x 300 method); one JSON object."""
+    import torch
+
+    import layer_gram_embedding_gb300 as ple
+    from layer_gram_embedding_gb300 import build as lib_build
+
+    lib_build.build()
+    device = torch.device("cuda", 0)
+    peaks, _ = measured_peaks()
+    out = []
+    for batch in wl.all_workloads():
+        def to_dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        T, B, L, H = batch.num_tokens, batch.num_requests, batch.num_layers, batch.num_heads
+        ids, ctx = to_dev(batch.ids), to_dev(batch.ngram_context)
+        M, vocab, off = (to_dev(batch.layer_multipliers), to_dev(batch.vocab_sizes),
+                         to_dev(batch.offsets))
+        cu = to_dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None
+        req = torch.empty(T, dtype=torch.int32, device=device)
+        local = torch.empty(T, dtype=torch.int32, device=device)
+        o = torch.empty((L, T, H), dtype=torch.int64, device=device)
+
+        def rows():
+            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
+                            batch.heads_per_ngram, batch.boundary_id, out=o)
+
+        def step():
+            ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
+            rows()
+
+        res = {"workload": batch.name + ("_i32" if batch.ids.dtype == np.int32 else ""),
+               "T": T, "B": B, "L": L, "H": H, "ngram_size": batch.ngram_size,
+               "row_ids_per_call": batch.row_ids_per_call,
+               "algorithmic_bytes": batch.algorithmic_bytes(), "launches_per_call": 1}
+        for name, fn in (("row_ids", rows), ("step", step)):
+            s = torch.cuda.Stream(device)
+            s.wait_stream(torch.cuda.current_stream(device))
+            with torch.cuda.stream(s):
+                fn()
+            torch.cuda.current_stream(device).wait_stream(s)
+            torch.cuda.synchronize(device)
+            g = torch.cuda.CUDAGraph()
+            calls = 300
+            with torch.cuda.graph(g):
+                for _ in range(calls):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize(device)
+            runs = []
+            for _ in range(7):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize(device)
+                runs.append(1e3 * e0.elapsed_time(e1) / calls)
+            us = statistics.median(runs)
+            res[f"{name}_us"] = us
+            del g
+        res["row_ids_per_s"] = batch.row_ids_per_call / (res["step_us"] / 1e6)
+        res["kernel_gbs"] = batch.algorithmic_bytes() / (res["row_ids_us"] / 1e6) / 1e9
+        res["kernel_frac_of_measured_hbm"] = res["kernel_gbs"] / peaks["hbm_gbs"]
+        out.append(res)
+        print(json.dumps(res), file=sys.stderr, flush=True)
+    print(json.dumps({"all_configs": out, "method": "CUDA graph of 300 back-to-back calls, "
+                      "median of 7 replays; step = ple_build_token_index + ple_row_ids"}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,11 +603,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of single-thread oracle work for cpu_baseline")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="time every workload (graph of 300 calls) instead of the contract line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.all_configs:
+        return all_configs(args)
     return our_arm(args)
 
 
