@@ -484,7 +484,9 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
 
 def decode_latency(ple, torch, device):
     """Device µs per call of ple_row_ids at decode B=1: a CUDA graph of 300
-    back-to-back calls, median of 7 replays (the page's 7 x 300 method)."""
+    back-to-back calls, median of 7 replays (the page's 7 x 300 method).
+    Measured without an index (req = local = NULL, one launch per step) and
+    with a prebuilt index (the page's memoized index)."""
     b = wl.decode(1)
 
     def to_dev(a):
@@ -494,29 +496,37 @@ def decode_latency(ple, torch, device):
     M, vocab, off = to_dev(b.layer_multipliers), to_dev(b.vocab_sizes), to_dev(b.offsets)
     req, local = ple.ple_build_token_index(None, 1, 1, True, device=device)
     out = torch.empty((1, 1, 4), dtype=torch.int64, device=device)
-    s = torch.cuda.Stream(device)
-    s.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(s):
-        ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
-    torch.cuda.current_stream(device).wait_stream(s)
-    torch.cuda.synchronize(device)
-    g = torch.cuda.CUDAGraph()
-    calls = 300
-    with torch.cuda.graph(g):
-        for _ in range(calls):
-            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
-    g.replay()
-    torch.cuda.synchronize(device)
-    per_call = []
-    for _ in range(7):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        g.replay()
-        e1.record()
+    res = {"launches_per_call": 1, "method": "CUDA graph of 300 calls, median of 7 replays"}
+    for name, (rq, lc) in (("device_us_per_call", (None, None)),
+                           ("device_us_per_call_with_index", (req, local))):
+        def call():
+            ple.ple_row_ids(ids, rq, lc, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
+
+        s = torch.cuda.Stream(device)
+        s.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(s):
+            call()
+        torch.cuda.current_stream(device).wait_stream(s)
         torch.cuda.synchronize(device)
-        per_call.append(1e3 * e0.elapsed_time(e1) / calls)
-    return {"device_us_per_call": statistics.median(per_call), "launches_per_call": 1,
-            "method": "CUDA graph of 300 calls, median of 7 replays", "runs_us": per_call}
+        g = torch.cuda.CUDAGraph()
+        calls = 300
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                call()
+        g.replay()
+        torch.cuda.synchronize(device)
+        per_call = []
+        for _ in range(7):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize(device)
+            per_call.append(1e3 * e0.elapsed_time(e1) / calls)
+        res[name] = statistics.median(per_call)
+        if name == "device_us_per_call":
+            res["runs_us"] = per_call
+    return res
 
 
 def all_configs(args):
@@ -544,9 +554,19 @@ def all_configs(args):
         req = torch.empty(T, dtype=torch.int32, device=device)
         local = torch.empty(T, dtype=torch.int32, device=device)
         o = torch.empty((L, T, H), dtype=torch.int64, device=device)
+        o32 = torch.empty((L, T, H), dtype=torch.int32, device=device)
 
         def rows():
             ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
+                            batch.heads_per_ngram, batch.boundary_id, out=o)
+
+        def rows_i32():
+            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
+                            batch.heads_per_ngram, batch.boundary_id, out=o32,
+                            out_dtype=torch.int32)
+
+        def rows_no_index():
+            ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, batch.ngram_size,
                             batch.heads_per_ngram, batch.boundary_id, out=o)
 
         def step():
@@ -557,7 +577,10 @@ def all_configs(args):
                "T": T, "B": B, "L": L, "H": H, "ngram_size": batch.ngram_size,
                "row_ids_per_call": batch.row_ids_per_call,
                "algorithmic_bytes": batch.algorithmic_bytes(), "launches_per_call": 1}
-        for name, fn in (("row_ids", rows), ("step", step)):
+        variants = [("row_ids", rows), ("step", step), ("row_ids_i32", rows_i32)]
+        if batch.is_decode:
+            variants.append(("row_ids_no_index", rows_no_index))
+        for name, fn in variants:
             s = torch.cuda.Stream(device)
             s.wait_stream(torch.cuda.current_stream(device))
             with torch.cuda.stream(s):
@@ -585,6 +608,10 @@ def all_configs(args):
         res["row_ids_per_s"] = batch.row_ids_per_call / (res["step_us"] / 1e6)
         res["kernel_gbs"] = batch.algorithmic_bytes() / (res["row_ids_us"] / 1e6) / 1e9
         res["kernel_frac_of_measured_hbm"] = res["kernel_gbs"] / peaks["hbm_gbs"]
+        bytes32 = batch.algorithmic_bytes() - 4 * L * T * H
+        res["i32_algorithmic_bytes"] = bytes32
+        res["i32_kernel_gbs"] = bytes32 / (res["row_ids_i32_us"] / 1e6) / 1e9
+        res["i32_kernel_frac_of_measured_hbm"] = res["i32_kernel_gbs"] / peaks["hbm_gbs"]
         out.append(res)
         print(json.dumps(res), file=sys.stderr, flush=True)
     print(json.dumps({"all_configs": out, "method": "CUDA graph of 300 back-to-back calls, "

@@ -112,6 +112,9 @@ ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests
  *                       order, so 0 <= local[t] <= t.  Values outside these
  *                       ranges are clamped into them: the kernel never reads
  *                       out of bounds, but such rows are unspecified.
+ *                       Both NULL: a decode batch (requires B == T), each
+ *                       token its own request at offset 0 -- the index is
+ *                       neither built nor read (one launch per step).
  *   ngram_context       [B, ctx_len], dtype id_dtype, device: each request's
  *                       last ctx_len ids before this batch, oldest first.
  *   num_requests        B >= 1 when T > 0.
@@ -132,8 +135,9 @@ ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests
  *   out                 [L, T, H] int64, device; every element is written.
  *
  * Errors: PLE_ERR_SIZE, PLE_ERR_GEOMETRY_CTX, PLE_ERR_GEOMETRY_HEADS (checked
- * in that order, before anything else), then PLE_ERR_NULL, PLE_ERR_DTYPE,
- * PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ * in that order, before anything else), then PLE_ERR_NULL (one of req /
+ * local NULL, or any other pointer), PLE_ERR_SIZE (both NULL with B != T),
+ * PLE_ERR_DTYPE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
  * One kernel launch; no host reads; fixed grid for fixed (T, L, H, N).
  */
 ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -142,6 +146,24 @@ ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_toke
                        const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
                        int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
                        int64_t boundary_id, int64_t* out, void* stream);
+
+/*
+ * ple_row_ids_i32 -- ple_row_ids with int32 row ids.
+ *
+ * The same operation, arguments, checks and launch as ple_row_ids, except
+ * that `out` is [L, T, H] int32 (4-byte aligned) and receives the low 32
+ * bits of each int64 row id (two's complement, as torch converts int64 to
+ * int32).  Row ids below 2^31 -- every table whose offsets plus vocab sizes
+ * stay below 2^31 -- are unchanged; the output bytes halve.  This is an
+ * opt-in variant: the page's row ids are int64 (section "What").
+ */
+ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                           const int32_t* req, const int32_t* local, const void* ngram_context,
+                           int32_t num_requests, int32_t ctx_len,
+                           const int64_t* layer_multipliers, const int64_t* vocab_sizes,
+                           const int64_t* offsets, int32_t num_heads, int32_t ngram_size,
+                           int32_t heads_per_ngram, int32_t num_layers, int64_t boundary_id,
+                           int32_t* out, void* stream);
 
 /*
  * ple_selftest_floor_mod -- diagnostic: the library's invariant-divisor

@@ -41,6 +41,8 @@ SIGNATURES = {
     "ple_build_token_index": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
     "ple_row_ids": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32, _I32,
                            _I32, _I64, _P, _P]),
+    "ple_row_ids_i32": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
+                               _I32, _I32, _I64, _P, _P]),
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
@@ -153,22 +155,29 @@ def ple_build_token_index(cu_seqlens, num_requests: int, num_tokens: int, is_dec
     return req, local
 
 
-def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor, local: torch.Tensor,
+def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.Tensor | None,
                 ngram_context: torch.Tensor, layer_multipliers: torch.Tensor,
                 vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
                 heads_per_ngram: int, boundary_id: int, out: torch.Tensor | None = None,
-                stream=None) -> torch.Tensor:
+                stream=None, out_dtype=torch.int64) -> torch.Tensor:
     """Row ids [L, T, H] int64 (one launch for every layer).
+
+    out_dtype=torch.int32 calls ple_row_ids_i32 instead: the low 32 bits of
+    each row id, half the output bytes.
 
     input_ids [T] and ngram_context [B, ngram_size-1]: int32 or int64, same
     dtype.  layer_multipliers [L, N] (or [N]), vocab_sizes and offsets
     [L, H] (or [H]): int64.  out: optional fixed [L, T, H] int64 destination
-    (a graph replay then writes into a stable buffer).  ValueError on the two
-    geometry preconditions and on tensors not all on one CUDA device.
+    (a graph replay then writes into a stable buffer).  req and local both
+    None: a decode batch (one token per request at offset 0, B == T), with no
+    index to build or read.  ValueError on the two geometry preconditions and
+    on tensors not all on one CUDA device.
     """
     where = "ple_row_ids"
-    dev = _one_cuda_device([input_ids, req, local, ngram_context, layer_multipliers, vocab_sizes,
-                            offsets] + ([out] if out is not None else []), where)
+    if (req is None) != (local is None):
+        raise ValueError(f"{where}: pass both req and local, or neither (decode)")
+    dev = _one_cuda_device([t for t in (input_ids, req, local, ngram_context, layer_multipliers,
+                                        vocab_sizes, offsets, out) if t is not None], where)
     if input_ids.dtype not in (torch.int32, torch.int64):
         raise TypeError(f"{where}: input_ids must be int32 or int64")
     if ngram_context.dtype != input_ids.dtype:
@@ -187,25 +196,31 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor, local: torch.Tensor,
     for name, t in (("input_ids", input_ids), ("ngram_context", ctx)):
         if not t.is_contiguous():
             raise ValueError(f"{where}: {name} must be contiguous")
-    for name, t in (("req", req), ("local", local)):
-        _need(t, torch.int32, name, where)
-        if t.numel() != T:
-            raise ValueError(f"{where}: {name} must be [T]")
+    if req is not None:
+        for name, t in (("req", req), ("local", local)):
+            _need(t, torch.int32, name, where)
+            if t.numel() != T:
+                raise ValueError(f"{where}: {name} must be [T]")
     for name, t in (("layer_multipliers", M), ("vocab_sizes", vocab), ("offsets", off)):
         _need(t, torch.int64, name, where)
     if M.shape != (L, N):
         raise ValueError(f"{where}: layer_multipliers must be [L, ngram_size]")
     if off.shape != (L, H):
         raise ValueError(f"{where}: offsets must have the shape of vocab_sizes")
+    if out_dtype not in (torch.int64, torch.int32):
+        raise TypeError(f"{where}: out_dtype must be torch.int64 or torch.int32")
     if out is None:
-        out = torch.empty((L, T, H), dtype=torch.int64, device=dev)
+        out = torch.empty((L, T, H), dtype=out_dtype, device=dev)
     else:
-        _need(out, torch.int64, "out", where)
+        _need(out, out_dtype, "out", where)
         if tuple(out.shape) not in ((L, T, H),) + (((T, H),) if L == 1 else ()):
             raise ValueError(f"{where}: out must be [L, T, H]")
     dtype_code = PLE_I64 if input_ids.dtype == torch.int64 else PLE_I32
     with torch.cuda.device(dev):
-        st = lib().ple_row_ids(_ptr(input_ids), dtype_code, T, _ptr(req), _ptr(local), _ptr(ctx),
+        fn = lib().ple_row_ids if out_dtype == torch.int64 else lib().ple_row_ids_i32
+        st = fn(_ptr(input_ids), dtype_code, T,
+                               _ptr(req) if req is not None else ctypes.c_void_p(0),
+                               _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx),
                                ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
                                int(heads_per_ngram), L, int(boundary_id), _ptr(out),
                                _stream_handle(stream, dev))

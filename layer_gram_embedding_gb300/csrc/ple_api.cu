@@ -74,14 +74,14 @@ extern "C" ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t n
     return PLE_OK;
 }
 
-extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
-                                  const int32_t* req, const int32_t* local,
-                                  const void* ngram_context, int32_t num_requests,
-                                  int32_t ctx_len, const int64_t* layer_multipliers,
-                                  const int64_t* vocab_sizes, const int64_t* offsets,
-                                  int32_t num_heads, int32_t ngram_size, int32_t heads_per_ngram,
-                                  int32_t num_layers, int64_t boundary_id, int64_t* out,
-                                  void* stream) {
+namespace {
+
+ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                        const int32_t* req, const int32_t* local, const void* ngram_context,
+                        int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
+                        const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
+                        int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
+                        int64_t boundary_id, void* out, int out_bytes, void* stream) {
     // sizes first, then the page's two geometry preconditions
     if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
         num_tokens < 0 || num_tokens > INT32_MAX)
@@ -92,14 +92,17 @@ extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64
     if (num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
     if (num_tokens == 0) return PLE_OK;
     if (num_requests < 1) return PLE_ERR_SIZE;
-    if (!input_ids || !req || !local || !ngram_context || !layer_multipliers || !vocab_sizes ||
-        !offsets || !out)
+    // both index pointers NULL: a decode batch, one token per request at offset 0
+    const bool index_free = !req && !local;
+    if (index_free && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
+    if (!input_ids || (!index_free && (!req || !local)) || !ngram_context || !layer_multipliers ||
+        !vocab_sizes || !offsets || !out)
         return PLE_ERR_NULL;
     if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
         !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
-        !aligned(offsets, 8) || !aligned(out, 8))
+        !aligned(offsets, 8) || !aligned(out, out_bytes))
         return PLE_ERR_ALIGN;
 
     (void)cudaGetLastError();
@@ -125,11 +128,41 @@ extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64
     p.L = num_layers;
     p.ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
     p.out_vec_ok = aligned(out, 16) ? 1 : 0;
+    p.index_free = index_free ? 1 : 0;
+    p.out_bytes = out_bytes;
     const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev);
     if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
     e = ple::launch_row_ids(p, id_bytes, cfg, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_failure(e);
     return PLE_OK;
+}
+
+}  // namespace
+
+extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                                  const int32_t* req, const int32_t* local,
+                                  const void* ngram_context, int32_t num_requests,
+                                  int32_t ctx_len, const int64_t* layer_multipliers,
+                                  const int64_t* vocab_sizes, const int64_t* offsets,
+                                  int32_t num_heads, int32_t ngram_size, int32_t heads_per_ngram,
+                                  int32_t num_layers, int64_t boundary_id, int64_t* out,
+                                  void* stream) {
+    return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
+                        ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
+                        heads_per_ngram, num_layers, boundary_id, out, 8, stream);
+}
+
+extern "C" ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                                      const int32_t* req, const int32_t* local,
+                                      const void* ngram_context, int32_t num_requests,
+                                      int32_t ctx_len, const int64_t* layer_multipliers,
+                                      const int64_t* vocab_sizes, const int64_t* offsets,
+                                      int32_t num_heads, int32_t ngram_size,
+                                      int32_t heads_per_ngram, int32_t num_layers,
+                                      int64_t boundary_id, int32_t* out, void* stream) {
+    return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
+                        ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
+                        heads_per_ngram, num_layers, boundary_id, out, 4, stream);
 }
 
 extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,

@@ -32,7 +32,7 @@ struct RowIdsParams {
     const int64_t* mult;    // [L, N]
     const int64_t* vocab;   // [L, H]
     const int64_t* offsets; // [L, H]
-    int64_t* out;           // [L, T, H]
+    void* out;              // [L, T, H] int64 or int32 (out_bytes)
     int64_t T;
     int64_t boundary;
     int32_t B;
@@ -44,6 +44,8 @@ struct RowIdsParams {
     int32_t stage_pitch;    // row pitch (in int64) of the output staging tile
     int32_t ids_vec_ok;     // ids pointer is 16-byte aligned
     int32_t out_vec_ok;     // out pointer is 16-byte aligned
+    int32_t index_free;     // decode without an index: req[t] = t, local[t] = 0
+    int32_t out_bytes;      // 8: int64 row ids, 4: their low 32 bits
 };
 
 struct RowIdsLaunch {

@@ -167,7 +167,10 @@ __device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids
                                        int i, bool live, int N, int64_t (&V)[NMAX]) {
     const int64_t t = t0 + i;
     int32_t r = 0, q = 0;
-    if (live) {
+    if (p.index_free) {
+        // a decode batch without an index: every token is its own request
+        r = (int32_t)t;
+    } else if (live) {
         r = __ldg(p.req + t);
         q = __ldg(p.local + t);
     }
@@ -210,9 +213,11 @@ __device__ __forceinline__ void hash_layer(const int64_t (&V)[NMAX], int N, int 
 }
 
 // Runtime-shape readout of one staged half tile (nsub tokens x H int64, row
-// pitch `pitch`): 8-byte units in global order, incremental (row, column).
+// pitch `pitch`): one element per lane per step in global order, incremental
+// (row, column).  An int32 destination receives each row id's low 32 bits.
+template <typename OutT>
 __device__ __forceinline__ void readout_runtime(const int64_t* __restrict__ stage,
-                                                long long* __restrict__ dst, int lane, int nsub,
+                                                OutT* __restrict__ dst, int lane, int nsub,
                                                 int H, int pitch) {
     const int dq = 32 / H;
     const int dr = 32 % H;
@@ -220,7 +225,10 @@ __device__ __forceinline__ void readout_runtime(const int64_t* __restrict__ stag
     int rr = lane % H;
     const int nel = nsub * H;
     for (int e = lane; e < nel; e += 32) {
-        __stcs(dst + e, (long long)stage[qq * pitch + rr]);
+        if constexpr (sizeof(OutT) == 8)
+            __stcs(reinterpret_cast<long long*>(dst) + e, (long long)stage[qq * pitch + rr]);
+        else
+            __stcs(reinterpret_cast<int*>(dst) + e, (int)stage[qq * pitch + rr]);
         rr += dr;
         qq += dq;
         if (rr >= H) {
@@ -231,7 +239,7 @@ __device__ __forceinline__ void readout_runtime(const int64_t* __restrict__ stag
 }
 
 // Any shape: one token per lane per half tile, int64 staging with odd pitch.
-template <typename IdT, int NT>
+template <typename IdT, int NT, typename OutT>
 __global__ void __launch_bounds__(kMaxWarps * 32)
 row_ids_kernel(const RowIdsParams p) {
     constexpr int NMAX = NT > 0 ? NT : PLE_MAX_NGRAM;
@@ -275,9 +283,8 @@ row_ids_kernel(const RowIdsParams p) {
                 hash_layer<NMAX, NT, false>(V, N, hpn, sm.mul + l * N, sm.fast + hb, sm.off + hb,
                                             sm.ext + hb, stage + lane * pitch);
             __syncwarp();
-            long long* dst = reinterpret_cast<long long*>(p.out) +
-                             ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
-            readout_runtime(stage, dst, lane, nsub, H, pitch);
+            OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
+            readout_runtime<OutT>(stage, dst, lane, nsub, H, pitch);
             __syncwarp();
         }
     }
@@ -314,7 +321,36 @@ __device__ __forceinline__ void readout_pairs(const uint2* __restrict__ st,
     }
 }
 
-template <typename IdT, int NT, int HPT>
+// int32 row ids: four heads (two staged pairs) per 16-byte lane store; the
+// offsets' low words are added in 32-bit arithmetic (the low 32 bits of the
+// int64 row id).  K2 quads per token.
+template <int K2, int P2, int NC, int GSTEP, bool kVec, bool kFull>
+__device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int* __restrict__ dst,
+                                              int lane, int nsub, const int (&soff)[K2],
+                                              const int (&stok)[K2], const int4 (&offs)[NC]) {
+    int4* d4 = reinterpret_cast<int4*>(dst);
+#pragma unroll
+    for (int j = 0; j < K2; ++j) {
+        if (kFull || stok[j] < nsub) {
+            const uint2 a = st[soff[j]];
+            const uint2 b = st[soff[j] + 1];
+            const int4 o = offs[((32 * j) % K2) / GSTEP];
+            const int4 rows = make_int4((int)((unsigned)o.x + a.x), (int)((unsigned)o.y + a.y),
+                                        (int)((unsigned)o.z + b.x), (int)((unsigned)o.w + b.y));
+            if (kVec) {
+                __stcs(d4 + 32 * j + lane, rows);
+            } else {
+                int* d1 = reinterpret_cast<int*>(d4 + 32 * j + lane);
+                __stcs(d1, rows.x);
+                __stcs(d1 + 1, rows.y);
+                __stcs(d1 + 2, rows.z);
+                __stcs(d1 + 3, rows.w);
+            }
+        }
+    }
+}
+
+template <typename IdT, int NT, int HPT, typename OutT>
 __global__ void __launch_bounds__(kMaxWarps * 32)
 row_ids_fixed_kernel(const RowIdsParams p) {
     static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
@@ -323,8 +359,6 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     constexpr int K = H / 2;        // 16-byte output chunks (head pairs) per token
     constexpr int P2 = K | 1;       // staging row pitch in 8-byte pairs (odd)
     constexpr int PG = H | 1;       // int64 staging pitch for the general path (odd)
-    constexpr int GSTEP = gcd_const(32, K);  // the steps (32 j) % K are its multiples
-    constexpr int NC = K / GSTEP;   // distinct readout columns per lane
     static_assert(K <= 32, "readout walk assumes K <= 32");
     const int G = p.group_layers;
     const int l0 = blockIdx.y * G;
@@ -367,9 +401,9 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                 hash_layer<N, N, false>(u == 0 ? VA : VB, N, HPT, sm.mul + l * N, sm.fast + hb,
                                         sm.off + hb, sm.ext + hb, st + lane * PG);
                 __syncwarp();
-                long long* dst = reinterpret_cast<long long*>(p.out) +
-                                 ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
-                readout_runtime(st, dst, lane, nsub, H, PG);
+                OutT* dst = static_cast<OutT*>(p.out) +
+                            ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
+                readout_runtime<OutT>(st, dst, lane, nsub, H, PG);
                 __syncwarp();
             }
         }
@@ -378,19 +412,25 @@ row_ids_fixed_kernel(const RowIdsParams p) {
 
     const uint2* stA = reinterpret_cast<const uint2*>(stage);
     uint2* stAw = reinterpret_cast<uint2*>(stage);
-    // readout walk, the same for every layer: chunk c = 32 j + lane of a half
-    // tile is token c / K, column c % K; with q0 = lane / K, r0 = lane % K the
-    // step j adds the compile-time (32 j) / K and (32 j) % K, carrying one
-    // token when the column wraps
-    const int q0 = lane / K;
-    const int r0 = lane % K;
-    int soff[K], stok[K];
+    // readout walk, the same for every layer: a 16-byte store carries U staged
+    // pairs (1 for int64, 2 for int32), KU such units per token; unit c =
+    // 32 j + lane of a half tile is token c / KU, column c % KU; with
+    // q0 = lane / KU, r0 = lane % KU the step j adds the compile-time
+    // (32 j) / KU and (32 j) % KU, carrying one token when the column wraps
+    constexpr int U = sizeof(OutT) == 8 ? 1 : 2;
+    static_assert(K % U == 0, "int32 output needs a multiple of 4 heads");
+    constexpr int KU = K / U;
+    constexpr int GU = gcd_const(32, KU);
+    constexpr int NU = KU / GU;
+    const int q0 = lane / KU;
+    const int r0 = lane % KU;
+    int soff[KU], stok[KU];
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
-        const int cj = (32 * j) % K;
-        const bool carry = r0 + cj >= K;
-        stok[j] = q0 + (32 * j) / K + (carry ? 1 : 0);
-        soff[j] = stok[j] * P2 + r0 + cj - (carry ? K : 0);
+    for (int j = 0; j < KU; ++j) {
+        const int cj = (32 * j) % KU;
+        const bool carry = r0 + cj >= KU;
+        stok[j] = q0 + (32 * j) / KU + (carry ? 1 : 0);
+        soff[j] = stok[j] * P2 + U * (r0 + cj - (carry ? KU : 0));
     }
     const bool full = nA == 32 && nB == 32;
     const bool vec_out = p.out_vec_ok != 0;
@@ -418,56 +458,83 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                     make_uint2(floormod_fast(uB, c0), floormod_fast(uB, c1));
             }
         }
-        // this lane's readout columns' offsets for layer l
-        longlong2 offs[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            int col = r0 + k * GSTEP;
-            col = col >= K ? col - K : col;
-            offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
-        }
         __syncwarp();
-        long long* dst = reinterpret_cast<long long*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
-        if (full && vec_out) {
-            readout_pairs<K, P2, NC, GSTEP, true, true>(stA, dst, lane, 32, soff, stok, offs);
-            readout_pairs<K, P2, NC, GSTEP, true, true>(stA + 32 * P2, dst + 32 * H, lane, 32,
-                                                       soff, stok, offs);
-        } else if (vec_out) {
-            readout_pairs<K, P2, NC, GSTEP, true, false>(stA, dst, lane, nA, soff, stok, offs);
-            if (nB > 0)
-                readout_pairs<K, P2, NC, GSTEP, true, false>(stA + 32 * P2, dst + 32 * H, lane,
-                                                            nB, soff, stok, offs);
+        OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
+        if constexpr (U == 1) {
+            // this lane's readout columns' offsets for layer l
+            longlong2 offs[NU];
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
+            }
+            long long* d = reinterpret_cast<long long*>(dst);
+            if (full && vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                         soff, stok, offs);
+            } else if (vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                              nB, soff, stok, offs);
+            } else {
+                readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                               nB, soff, stok, offs);
+            }
         } else {
-            readout_pairs<K, P2, NC, GSTEP, false, false>(stA, dst, lane, nA, soff, stok, offs);
-            if (nB > 0)
-                readout_pairs<K, P2, NC, GSTEP, false, false>(stA + 32 * P2, dst + 32 * H, lane,
-                                                             nB, soff, stok, offs);
+            int4 offs[NU];
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                const int64_t* o = sm.off + l * H + 4 * col;
+                offs[k] = make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]);
+            }
+            int* d = reinterpret_cast<int*>(dst);
+            if (full && vec_out) {
+                readout_quads<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                readout_quads<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                         soff, stok, offs);
+            } else if (vec_out) {
+                readout_quads<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quads<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                              nB, soff, stok, offs);
+            } else {
+                readout_quads<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quads<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                               nB, soff, stok, offs);
+            }
         }
         __syncwarp();
     }
 }
 
-template <typename IdT>
 using KernelFn = void (*)(const RowIdsParams);
 
 // Compile-time shapes: the PLE configurations this library is tuned for
 // (ngram_size, heads_per_ngram); everything else runs the runtime-shape
 // kernel for its ngram_size.
-template <typename IdT>
-KernelFn<IdT> pick_kernel(int N, int hpn) {
-    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2>;
-    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4>;
-    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4>;
-    if (N == 5 && hpn == 8) return row_ids_fixed_kernel<IdT, 5, 8>;
+template <typename IdT, typename OutT>
+KernelFn pick_kernel(int N, int hpn) {
+    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT>;
+    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT>;
+    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT>;
+    if (N == 5 && hpn == 8) return row_ids_fixed_kernel<IdT, 5, 8, OutT>;
     switch (N) {
-        case 2: return row_ids_kernel<IdT, 2>;
-        case 3: return row_ids_kernel<IdT, 3>;
-        case 4: return row_ids_kernel<IdT, 4>;
-        case 5: return row_ids_kernel<IdT, 5>;
-        case 6: return row_ids_kernel<IdT, 6>;
-        case 7: return row_ids_kernel<IdT, 7>;
-        case 8: return row_ids_kernel<IdT, 8>;
-        default: return row_ids_kernel<IdT, 0>;
+        case 2: return row_ids_kernel<IdT, 2, OutT>;
+        case 3: return row_ids_kernel<IdT, 3, OutT>;
+        case 4: return row_ids_kernel<IdT, 4, OutT>;
+        case 5: return row_ids_kernel<IdT, 5, OutT>;
+        case 6: return row_ids_kernel<IdT, 6, OutT>;
+        case 7: return row_ids_kernel<IdT, 7, OutT>;
+        case 8: return row_ids_kernel<IdT, 8, OutT>;
+        default: return row_ids_kernel<IdT, 0, OutT>;
     }
 }
 
@@ -475,9 +542,8 @@ bool shape_is_fixed(int N, int hpn) {
     return (N == 3 && (hpn == 2 || hpn == 4)) || (N == 4 && hpn == 4) || (N == 5 && hpn == 8);
 }
 
-template <typename IdT>
-cudaError_t launch_typed(const RowIdsParams& p, const RowIdsLaunch& cfg, cudaStream_t stream) {
-    const KernelFn<IdT> fn = pick_kernel<IdT>(p.N, p.hpn);
+cudaError_t launch_fn(KernelFn fn, const RowIdsParams& p, const RowIdsLaunch& cfg,
+                      cudaStream_t stream) {
     if (cfg.smem_bytes > 48 * 1024) {
         // Opting in to more than 48 KB of dynamic shared memory is a function
         // attribute; setting it is idempotent and not a stream operation.
@@ -541,8 +607,14 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev) {
 
 cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                            cudaStream_t stream) {
-    if (id_bytes == 4) return launch_typed<int32_t>(p, cfg, stream);
-    return launch_typed<int64_t>(p, cfg, stream);
+    KernelFn fn;
+    if (p.out_bytes == 4)
+        fn = id_bytes == 4 ? pick_kernel<int32_t, int32_t>(p.N, p.hpn)
+                           : pick_kernel<int64_t, int32_t>(p.N, p.hpn);
+    else
+        fn = id_bytes == 4 ? pick_kernel<int32_t, int64_t>(p.N, p.hpn)
+                           : pick_kernel<int64_t, int64_t>(p.N, p.hpn);
+    return launch_fn(fn, p, cfg, stream);
 }
 
 }  // namespace ple

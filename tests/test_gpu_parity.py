@@ -107,6 +107,51 @@ def test_row_ids_match_oracle_full_size(name):
     assert_same(gpu_rows(batch), oracle_rows(batch), name)
 
 
+def low32(a: np.ndarray) -> np.ndarray:
+    """The low 32 bits of int64 values as int32 (two's complement)."""
+    return (a.astype(np.uint64) & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.int32)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_int32_row_ids_full_size(name):
+    """ple_row_ids_i32: the low 32 bits of every row id."""
+    batch = WORKLOADS[name]
+    req, local = gpu_index(batch)
+    out = ple.ple_row_ids(dev(batch.ids), req, local, dev(batch.ngram_context),
+                          dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
+                          batch.ngram_size, batch.heads_per_ngram, batch.boundary_id,
+                          out_dtype=torch.int32)
+    assert out.dtype == torch.int32
+    assert_same(out, low32(oracle_rows(batch)), f"{name} int32")
+
+
+@pytest.mark.parametrize("chunk", range(3))
+def test_int32_row_ids_random_edges(chunk):
+    """Random offsets push row ids past 2^31 (the low words wrap); misaligned
+    outputs (4- but not 16-byte aligned) take the scalar stores."""
+    for seed in range(chunk * 40, (chunk + 1) * 40):
+        batch = wl.random_batch(9000 + seed, T_max=150,
+                                ids_dtype=np.int32 if seed % 2 else np.int64,
+                                N=[3, 4, 5, 3, 6][seed % 5], hpn=[2, 4, 8, 4, 3][seed % 5])
+        req, local = gpu_index(batch)
+        L, T, H = batch.num_layers, batch.num_tokens, batch.num_heads
+        buf = torch.full((L * T * H + 1,), 77, dtype=torch.int32, device=DEV)
+        out = buf[1:].view(L, T, H) if seed % 3 == 0 else buf[:-1].view(L, T, H)
+        ple.ple_row_ids(dev(batch.ids), req, local, dev(batch.ngram_context),
+                        dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
+                        batch.ngram_size, batch.heads_per_ngram, batch.boundary_id, out=out,
+                        out_dtype=torch.int32)
+        assert_same(out, low32(oracle_rows(batch)), f"int32 seed {seed}")
+
+
+def test_int32_row_ids_decode_without_index():
+    batch = wl.decode(8)
+    out = ple.ple_row_ids(dev(batch.ids), None, None, dev(batch.ngram_context),
+                          dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
+                          3, 2, batch.boundary_id, out_dtype=torch.int32)
+    assert_same(out, low32(oracle_rows(batch)), "int32 decode")
+
+
 @pytest.mark.parametrize("chunk", range(6))
 def test_random_edge_batches(chunk):
     """Small ragged batches spanning several 64-token tiles with ragged tails,
@@ -201,6 +246,50 @@ def test_per_layer_calls_with_row_pointers():
                              out.data_ptr(), stream)
         assert st == ple.PLE_OK
         assert torch.equal(out, full[l])
+
+
+@pytest.mark.parametrize("B", [1, 4, 8, 63, 64, 65, 1000])
+def test_decode_without_an_index(B):
+    """req = local = NULL: each token its own request at offset 0."""
+    batch = wl.decode(min(B, 8)) if B <= 8 else wl.random_batch(7000 + B, decode_batch=True,
+                                                                T_max=B, N=3, hpn=2, L=2)
+    if B > 8:
+        rng = np.random.default_rng(B)
+        batch.ids = rng.integers(0, wl.VOCAB, size=B, dtype=np.int64)
+        batch.ngram_context = rng.integers(0, wl.VOCAB, size=(B, 2), dtype=np.int64)
+        batch.ngram_context[rng.random((B, 2)) < 0.3] = batch.boundary_id
+    out = ple.ple_row_ids(dev(batch.ids), None, None, dev(batch.ngram_context),
+                          dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
+                          batch.ngram_size, batch.heads_per_ngram, batch.boundary_id)
+    assert_same(out, oracle_rows(batch), f"index-free decode B={B}")
+
+
+def test_decode_without_an_index_in_a_graph():
+    """One launch per decode step: capture once, replay with fresh ids."""
+    b0 = wl.decode(8)
+    ids, ctx = dev(b0.ids), dev(b0.ngram_context)
+    M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
+    out = torch.empty((1, 8, 4), dtype=torch.int64, device=DEV)
+
+    def step():
+        ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, 3, 2, b0.boundary_id, out=out)
+
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    torch.cuda.synchronize(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for replay in (1, 2, 3):
+        fresh = wl.decode(8, replay)
+        ids.copy_(dev(fresh.ids))
+        ctx.copy_(dev(fresh.ngram_context))
+        g.replay()
+        torch.cuda.synchronize(DEV)
+        assert_same(out, oracle_rows(fresh), f"index-free replay {replay}")
 
 
 @pytest.mark.parametrize("kind", ["decode_b1", "decode_b4", "decode_b8", "prefill_512"])

@@ -26,7 +26,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ple_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ple_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declarations_are_all_exported(lib):
@@ -82,6 +82,8 @@ def row_ids(lib, **kw):
     (dict(ids=None), ple.PLE_ERR_NULL),
     (dict(req=None), ple.PLE_ERR_NULL),
     (dict(local=None), ple.PLE_ERR_NULL),
+    (dict(req=None, local=None), ple.PLE_ERR_SIZE),          # index-free needs B == T
+    (dict(req=None, local=None, T=4, B=5), ple.PLE_ERR_SIZE),
     (dict(ctx=None), ple.PLE_ERR_NULL),
     (dict(M=None), ple.PLE_ERR_NULL),
     (dict(vocab=None), ple.PLE_ERR_NULL),
