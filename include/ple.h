@@ -166,6 +166,40 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
                            int32_t* out, void* stream);
 
 /*
+ * ple_row_ids_ex -- ple_row_ids with the output dtype chosen and the
+ * request contexts carried to the next call, in the same launch.
+ *
+ * The carried context is the state that section "What" (second observation)
+ * reads through ngram_context: each request's last ngram_size-1 ids before
+ * the batch.  After this call, next_context[r] holds the last ctx_len ids of
+ * (ngram_context[r], then request r's tokens of this batch), oldest first --
+ * what the request's next prefill chunk or decode step passes as its
+ * ngram_context.  A request with no token in the batch keeps its row.
+ *
+ *   all arguments up to boundary_id: as ple_row_ids.
+ *   out           [L, T, H] int64 (out_dtype PLE_I64) or int32 (PLE_I32, the
+ *                 low 32 bits as in ple_row_ids_i32), aligned to its element.
+ *   out_dtype     PLE_I64 or PLE_I32 (else PLE_ERR_DTYPE).
+ *   cu_seqlens    [B+1] int32, device, the batch layout the index was built
+ *                 from.  Required with next_context unless req = local = NULL
+ *                 (index-free decode, where every token ends its request);
+ *                 ignored without next_context.
+ *   next_context  optional [B, ctx_len] output, dtype id_dtype, device; NULL
+ *                 for no carry.  Must not overlap ngram_context (the kernel
+ *                 reads every context row while it writes).
+ *
+ * Errors: as ple_row_ids, plus PLE_ERR_DTYPE for out_dtype and PLE_ERR_NULL
+ * for a carry without cu_seqlens outside an index-free decode.
+ */
+ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                          const int32_t* req, const int32_t* local, const void* ngram_context,
+                          int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
+                          const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
+                          int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
+                          int64_t boundary_id, void* out, int32_t out_dtype,
+                          const int32_t* cu_seqlens, void* next_context, void* stream);
+
+/*
  * ple_selftest_floor_mod -- diagnostic: the library's invariant-divisor
  * floored remainder next to one computed with CUDA's own % operator.
  *

@@ -43,6 +43,8 @@ SIGNATURES = {
                            _I32, _I64, _P, _P]),
     "ple_row_ids_i32": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
                                _I32, _I32, _I64, _P, _P]),
+    "ple_row_ids_ex": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
+                              _I32, _I32, _I64, _P, _I32, _P, _P, _P]),
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
@@ -159,11 +161,15 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                 ngram_context: torch.Tensor, layer_multipliers: torch.Tensor,
                 vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
                 heads_per_ngram: int, boundary_id: int, out: torch.Tensor | None = None,
-                stream=None, out_dtype=torch.int64) -> torch.Tensor:
+                stream=None, out_dtype=torch.int64, cu_seqlens: torch.Tensor | None = None,
+                next_context: torch.Tensor | None = None) -> torch.Tensor:
     """Row ids [L, T, H] int64 (one launch for every layer).
 
     out_dtype=torch.int32 calls ple_row_ids_i32 instead: the low 32 bits of
-    each row id, half the output bytes.
+    each row id, half the output bytes.  next_context ([B, ngram_size-1],
+    dtype of the ids, not overlapping ngram_context) receives each request's
+    carried context in the same launch (ple_row_ids_ex); it needs cu_seqlens
+    unless req and local are None (index-free decode).
 
     input_ids [T] and ngram_context [B, ngram_size-1]: int32 or int64, same
     dtype.  layer_multipliers [L, N] (or [N]), vocab_sizes and offsets
@@ -217,13 +223,27 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
             raise ValueError(f"{where}: out must be [L, T, H]")
     dtype_code = PLE_I64 if input_ids.dtype == torch.int64 else PLE_I32
     with torch.cuda.device(dev):
-        fn = lib().ple_row_ids if out_dtype == torch.int64 else lib().ple_row_ids_i32
-        st = fn(_ptr(input_ids), dtype_code, T,
-                               _ptr(req) if req is not None else ctypes.c_void_p(0),
-                               _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx),
-                               ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
-                               int(heads_per_ngram), L, int(boundary_id), _ptr(out),
-                               _stream_handle(stream, dev))
+        common = (_ptr(input_ids), dtype_code, T,
+                  _ptr(req) if req is not None else ctypes.c_void_p(0),
+                  _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx),
+                  ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
+                  int(heads_per_ngram), L, int(boundary_id), _ptr(out))
+        if next_context is None:
+            fn = lib().ple_row_ids if out_dtype == torch.int64 else lib().ple_row_ids_i32
+            st = fn(*common, _stream_handle(stream, dev))
+        else:
+            if next_context.dtype != input_ids.dtype or tuple(next_context.shape) != tuple(ctx.shape):
+                raise ValueError(f"{where}: next_context must be [B, ngram_size-1] of the ids' dtype")
+            if not next_context.is_contiguous() or next_context.device != dev:
+                raise ValueError(f"{where}: next_context must be contiguous, on the ids' device")
+            if cu_seqlens is not None:
+                _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+                if cu_seqlens.device != dev or cu_seqlens.numel() != ctx.shape[0] + 1:
+                    raise ValueError(f"{where}: cu_seqlens must be [B + 1] on the ids' device")
+            st = lib().ple_row_ids_ex(*common, PLE_I64 if out_dtype == torch.int64 else PLE_I32,
+                                      _ptr(cu_seqlens) if cu_seqlens is not None
+                                      else ctypes.c_void_p(0), _ptr(next_context),
+                                      _stream_handle(stream, dev))
     _check(st, where)
     return out
 

@@ -81,7 +81,8 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
                         int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
                         const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
                         int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
-                        int64_t boundary_id, void* out, int out_bytes, void* stream) {
+                        int64_t boundary_id, void* out, int out_bytes, const int32_t* cu_seqlens,
+                        void* next_context, void* stream) {
     // sizes first, then the page's two geometry preconditions
     if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
         num_tokens < 0 || num_tokens > INT32_MAX)
@@ -90,6 +91,7 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     if ((int64_t)num_heads != (int64_t)(ngram_size - 1) * heads_per_ngram)
         return PLE_ERR_GEOMETRY_HEADS;
     if (num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
+    if (out_bytes != 4 && out_bytes != 8) return PLE_ERR_DTYPE;
     if (num_tokens == 0) return PLE_OK;
     if (num_requests < 1) return PLE_ERR_SIZE;
     // both index pointers NULL: a decode batch, one token per request at offset 0
@@ -98,11 +100,15 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     if (!input_ids || (!index_free && (!req || !local)) || !ngram_context || !layer_multipliers ||
         !vocab_sizes || !offsets || !out)
         return PLE_ERR_NULL;
+    // the carry finds each request's last token (and empty requests) through
+    // cu_seqlens, except in an index-free decode
+    if (next_context && !index_free && !cu_seqlens) return PLE_ERR_NULL;
     if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
         !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
-        !aligned(offsets, 8) || !aligned(out, out_bytes))
+        !aligned(offsets, 8) || !aligned(out, out_bytes) || !aligned(cu_seqlens, 4) ||
+        !aligned(next_context, id_bytes))
         return PLE_ERR_ALIGN;
 
     (void)cudaGetLastError();
@@ -130,6 +136,8 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     p.out_vec_ok = aligned(out, 16) ? 1 : 0;
     p.index_free = index_free ? 1 : 0;
     p.out_bytes = out_bytes;
+    p.cu = next_context ? cu_seqlens : nullptr;
+    p.next_ctx = next_context;
     const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev);
     if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
     e = ple::launch_row_ids(p, id_bytes, cfg, static_cast<cudaStream_t>(stream));
@@ -149,7 +157,8 @@ extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64
                                   void* stream) {
     return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
-                        heads_per_ngram, num_layers, boundary_id, out, 8, stream);
+                        heads_per_ngram, num_layers, boundary_id, out, 8, nullptr, nullptr,
+                        stream);
 }
 
 extern "C" ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -162,7 +171,25 @@ extern "C" ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, i
                                       int64_t boundary_id, int32_t* out, void* stream) {
     return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
-                        heads_per_ngram, num_layers, boundary_id, out, 4, stream);
+                        heads_per_ngram, num_layers, boundary_id, out, 4, nullptr, nullptr,
+                        stream);
+}
+
+extern "C" ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                                     const int32_t* req, const int32_t* local,
+                                     const void* ngram_context, int32_t num_requests,
+                                     int32_t ctx_len, const int64_t* layer_multipliers,
+                                     const int64_t* vocab_sizes, const int64_t* offsets,
+                                     int32_t num_heads, int32_t ngram_size,
+                                     int32_t heads_per_ngram, int32_t num_layers,
+                                     int64_t boundary_id, void* out, int32_t out_dtype,
+                                     const int32_t* cu_seqlens, void* next_context,
+                                     void* stream) {
+    const int out_bytes = out_dtype == PLE_I32 ? 4 : out_dtype == PLE_I64 ? 8 : 0;
+    return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
+                        ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
+                        heads_per_ngram, num_layers, boundary_id, out, out_bytes, cu_seqlens,
+                        next_context, stream);
 }
 
 extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,

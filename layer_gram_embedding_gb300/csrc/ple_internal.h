@@ -46,6 +46,8 @@ struct RowIdsParams {
     int32_t out_vec_ok;     // out pointer is 16-byte aligned
     int32_t index_free;     // decode without an index: req[t] = t, local[t] = 0
     int32_t out_bytes;      // 8: int64 row ids, 4: their low 32 bits
+    const int32_t* cu;      // [B+1] cu_seqlens, for the context carry (NULL: decode)
+    void* next_ctx;         // [B, N-1] carried context out, dtype of ids (NULL: none)
 };
 
 struct RowIdsLaunch {
@@ -66,6 +68,10 @@ cudaError_t device_facts(DeviceFacts* out);
 RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev);
 cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                            cudaStream_t stream);
+// The tuned (ngram_size, heads_per_ngram) pairs of the fixed-shape kernel.
+bool shape_is_fixed(int N, int hpn);
+cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                                 cudaStream_t stream);
 
 cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                int32_t* req, int32_t* local, const DeviceFacts& dev,

@@ -1,0 +1,316 @@
+// The PLE n-gram row-id hash on sm_103a: device code shared by the fixed-shape
+// kernel (ple_rowids_fixed.cu) and the runtime-shape kernel
+// (ple_rowids_runtime.cu).
+//
+// Computes, for every token of a ragged batch and every layer, head and
+// n-gram order, the table row id of FreeToken PR #338 ("perf(ple): fuse the
+// n-gram row-id hash into one Triton kernel", section "What"):
+//
+//   V(t,s) = W(t,s) while no boundary id lies among W(t,1..s), else the
+//            boundary id (first observation: the whole-window cummax scan
+//            only ever looks ngram_size-1 places back, so the predicate is
+//            carried over at most ngram_size-1 steps);
+//   W(t,s) = ids[t-s] if local[t] >= s, else the carried context
+//            ngram_context[req[t]][ctx_len + local[t] - s] (second
+//            observation: the packed window is never built);
+//   row    = floormod(XOR_{s<n} V(t,s)*M[l][s], vocab[l][h]) + off[l][h].
+//
+// Work decomposition (one GPU, HBM-bound: 8*L*H bytes of row ids are written
+// per token against 16 bytes read):
+//   - grid.x covers the tokens in warp tiles of 64; grid.y splits the layers
+//     into groups so that even a small T fills the SMs.
+//   - Block prologue: the group's per-head divisor constants (one reciprocal
+//     per head, see ple_divmod.cuh) and multipliers go to shared memory.
+//   - Each warp stages its tile's ids plus an ngram_size-1 halo in shared
+//     memory (16-byte vector loads when aligned) and builds each token's
+//     window V in registers with the carried boundary predicate.
+//   - Fixed shapes (the tuned (ngram_size, heads_per_ngram) pairs, even
+//     heads per order): each lane hashes two tokens per shared constant load,
+//     stages 32-bit remainders as head pairs in rows of odd pitch (8-byte
+//     stores hit 16 distinct bank pairs per half warp), and the readout walks
+//     the tile in global order ([L, T, H]), adds each head's offset in
+//     registers and stores 16 bytes per lane: a warp store covers 512
+//     consecutive bytes.
+//   - Any other shape: one token per lane, int64 rows staged with odd pitch,
+//     8-byte readout.  Heads off the 32-bit fast path (vocab outside
+//     (0, 2^29]) use the same int64 staging in either kernel.
+//   - No inter-warp communication after the prologue (warp-per-tile), no
+//     atomics, no host reads: the launch is graph-capturable.
+#pragma once
+
+#include <stdint.h>
+
+#include "ple.h"
+#include "ple_divmod.cuh"
+#include "ple_internal.h"
+
+namespace ple {
+namespace {
+
+
+template <typename IdT>
+__device__ __forceinline__ int64_t load_id(const IdT* p, int64_t i);
+
+template <>
+__device__ __forceinline__ int64_t load_id<int64_t>(const int64_t* p, int64_t i) {
+    return (int64_t)__ldg(reinterpret_cast<const long long*>(p) + i);
+}
+
+template <>
+__device__ __forceinline__ int64_t load_id<int32_t>(const int32_t* p, int64_t i) {
+    return (int64_t)__ldg(p + i);
+}
+
+// A full 64-token tile of ids, 16-byte vector loads (tile base 16B-aligned).
+template <typename IdT>
+__device__ __forceinline__ void load_tile_vec(const IdT* src, int64_t* dst, int lane);
+
+template <>
+__device__ __forceinline__ void load_tile_vec<int64_t>(const int64_t* src, int64_t* dst, int lane) {
+    // 64 ids = 512 bytes = one 16-byte load per lane
+    const longlong2 v = __ldg(reinterpret_cast<const longlong2*>(src) + lane);
+    reinterpret_cast<longlong2*>(dst)[lane] = v;
+}
+
+template <>
+__device__ __forceinline__ void load_tile_vec<int32_t>(const int32_t* src, int64_t* dst, int lane) {
+    // 64 ids = 256 bytes = one 16-byte load for each of 16 lanes
+    if (lane < 16) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(src) + lane);
+        longlong2* d = reinterpret_cast<longlong2*>(dst) + 2 * lane;
+        d[0] = make_longlong2((long long)v.x, (long long)v.y);
+        d[1] = make_longlong2((long long)v.z, (long long)v.w);
+    }
+}
+
+// Per-block shared-memory layout, in order (all offsets 16-byte aligned):
+//   head constants of the layer group, structure of arrays:
+//     fast [G*H] uint4, off [G*H] int64 (padded to even), ext [G*H] uint4
+//   multipliers [G*N] int64 (padded to even)
+//   per warp: ids [kHaloSlots + kTileTokens] int64
+//   per warp: staging, stage_bytes(...) bytes
+struct SmemLayout {
+    uint4* fast;
+    int64_t* off;
+    uint4* ext;
+    int64_t* mul;
+    int64_t* ids;
+    unsigned char* stage;
+};
+
+__host__ __device__ constexpr size_t head_const_bytes(int heads) {
+    return (size_t)heads * 16 + (size_t)((heads + 1) & ~1) * 8 + (size_t)heads * 16;
+}
+
+// Staging bytes per warp.  Fixed shapes (even heads_per_ngram): 64 rows of
+// 32-bit remainders in 8-byte pairs, odd pitch (H/2 | 1) pairs, or 32 rows of
+// int64 rows with odd pitch (H | 1) for heads off the fast path -- whichever
+// is larger.  Runtime shapes: 32 rows of int64 with odd pitch.
+__host__ __device__ constexpr size_t stage_bytes(int H, bool fixed_shape) {
+    return fixed_shape ? ((size_t)64 * ((H / 2) | 1) * 8 > (size_t)32 * (H | 1) * 8
+                              ? (size_t)64 * ((H / 2) | 1) * 8
+                              : (size_t)32 * (H | 1) * 8)
+                       : (size_t)32 * (H | 1) * 8;
+}
+
+__device__ __forceinline__ SmemLayout carve_smem(unsigned char* base, int G, int H, int N,
+                                                 int nwarps) {
+    SmemLayout s;
+    const int gh = G * H;
+    s.fast = reinterpret_cast<uint4*>(base);
+    s.off = reinterpret_cast<int64_t*>(base + (size_t)gh * 16);
+    s.ext = reinterpret_cast<uint4*>(base + (size_t)gh * 16 + (size_t)((gh + 1) & ~1) * 8);
+    s.mul = reinterpret_cast<int64_t*>(base + head_const_bytes(gh));
+    s.ids = s.mul + ((G * N + 1) & ~1);
+    s.stage = reinterpret_cast<unsigned char*>(s.ids + nwarps * (kHaloSlots + kTileTokens));
+    return s;
+}
+
+// Block prologue: the layer group's head constants and multipliers.
+// Returns this thread's vote on whether every head takes the 32-bit fast
+// path; the caller publishes the constants with __syncthreads_and once its
+// own window loads are in flight, so the per-head divisions overlap them.
+__device__ __forceinline__ int load_group_constants(const RowIdsParams& p, const SmemLayout& sm,
+                                                    int l0, int gl, int H, int N) {
+    int fast = 1;
+    for (int i = threadIdx.x; i < gl * H; i += blockDim.x) {
+        const int64_t k = (int64_t)l0 * H + i;
+        const HeadConst c = make_head_const(p.vocab[k], p.offsets[k]);
+        sm.fast[i] = c.fast;
+        sm.off[i] = c.off;
+        sm.ext[i] = c.ext;
+        fast &= (c.ext.z == kHeadFast) ? 1 : 0;
+    }
+    for (int i = threadIdx.x; i < gl * N; i += blockDim.x) sm.mul[i] = p.mult[(int64_t)l0 * N + i];
+    return fast;
+}
+
+// Programmatic dependent launch: the row-id kernel may be scheduled while
+// the kernel before it in the stream drains, so it waits for that grid's
+// completion (and memory) before its first global read.  Without the launch
+// attribute this returns at once.
+__device__ __forceinline__ void wait_prior_grid() { cudaGridDependencySynchronize(); }
+
+// Stage a warp tile's ids (and the N-1 ids left of it) in shared memory.
+template <typename IdT>
+__device__ __forceinline__ void stage_ids(const RowIdsParams& p, int64_t* ids_s, int64_t t0,
+                                          int ntile, int N, int lane) {
+    const IdT* ids = static_cast<const IdT*>(p.ids);
+    if (ntile == kTileTokens && p.ids_vec_ok) {
+        load_tile_vec<IdT>(ids + t0, ids_s, lane);
+    } else {
+        for (int i = lane; i < ntile; i += 32) ids_s[i] = load_id<IdT>(ids, t0 + i);
+    }
+    if (lane < N - 1 && t0 - 1 - lane >= 0) ids_s[-1 - lane] = load_id<IdT>(ids, t0 - 1 - lane);
+    __syncwarp();
+}
+
+// The shifted window V(t, 0..N-1) of tile token i with the carried boundary
+// predicate.  Index data outside the addressable ranges is clamped; the
+// clamped request and offset are returned for the context carry.  The
+// index-free decode is a compile-time choice: a run-time branch here costs
+// the large-prefill kernel about 3% (measured on GB300).
+template <typename IdT, int NMAX, int NT, bool kIndexFree>
+__device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids_s, int64_t t0,
+                                       int i, bool live, int N, int64_t (&V)[NMAX],
+                                       int32_t& r_out, int32_t& q_out) {
+    const int64_t t = t0 + i;
+    int32_t r = 0, q = 0;
+    if (kIndexFree) {
+        // a decode batch without an index: every token is its own request
+        r = (int32_t)t;
+    } else if (live) {
+        r = __ldg(p.req + t);
+        q = __ldg(p.local + t);
+    }
+    r = min(max(r, 0), p.B - 1);
+    q = (int32_t)min((int64_t)max(q, 0), t);
+    r_out = r;
+    q_out = q;
+    V[0] = live ? ids_s[i] : 0;
+    const IdT* crow = static_cast<const IdT*>(p.ctx) + (int64_t)r * (N - 1) + (N - 1) + q;
+    bool valid = true;
+#pragma unroll
+    for (int s = 1; s < NMAX; ++s) {
+        if (NT == 0 && s >= N) break;
+        const int64_t w = (q >= s) ? ids_s[i - s] : load_id<IdT>(crow, -s);
+        valid = valid && (w != p.boundary);
+        V[s] = valid ? w : p.boundary;
+    }
+}
+
+// The context carry: the last token of each request writes the request's
+// next ngram_context row, the last N-1 ids of (context row, this batch's
+// tokens) = W(t, N-2), ..., W(t, 0), oldest first.  Without cu_seqlens
+// (index-free decode) every token is the last of its request.
+template <typename IdT>
+__device__ __forceinline__ void carry_context(const RowIdsParams& p, const int64_t* ids_s,
+                                              int64_t t0, int i, bool live, int N, int32_t r,
+                                              int32_t q) {
+    if (!live) return;
+    const int64_t t = t0 + i;
+    if (p.cu != nullptr && t != (int64_t)__ldg(p.cu + r + 1) - 1) return;
+    const IdT* crow = static_cast<const IdT*>(p.ctx) + (int64_t)r * (N - 1) + (N - 1) + q;
+    IdT* dst = static_cast<IdT*>(p.next_ctx) + (int64_t)r * (N - 1);
+    for (int c = 0; c < N - 1; ++c) {
+        const int s = N - 2 - c;
+        dst[c] = (q >= s) ? (IdT)ids_s[i - s] : crow[-s];
+    }
+}
+
+// Requests with no token in this batch keep their context row.  Needs
+// cu_seqlens; run by the blocks of the first layer group.
+template <typename IdT>
+__device__ __forceinline__ void carry_empty_requests(const RowIdsParams& p, int N) {
+    if (p.next_ctx == nullptr || p.cu == nullptr || blockIdx.y != 0) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.B; r += stride) {
+        if (__ldg(p.cu + r) == __ldg(p.cu + r + 1)) {
+            const IdT* src = static_cast<const IdT*>(p.ctx) + r * (N - 1);
+            IdT* dst = static_cast<IdT*>(p.next_ctx) + r * (N - 1);
+            for (int c = 0; c < N - 1; ++c) dst[c] = src[c];
+        }
+    }
+}
+
+// Hash one layer for one token into its int64 staging row (8-byte stores).
+template <int NMAX, int NT, bool kFast>
+__device__ __forceinline__ void hash_layer(const int64_t (&V)[NMAX], int N, int hpn,
+                                           const int64_t* __restrict__ ml,
+                                           const uint4* __restrict__ hf,
+                                           const int64_t* __restrict__ ho,
+                                           const uint4* __restrict__ he,
+                                           int64_t* __restrict__ srow) {
+    uint64_t mix = (uint64_t)V[0] * (uint64_t)ml[0];
+#pragma unroll
+    for (int s = 1; s < NMAX; ++s) {
+        if (NT == 0 && s >= N) break;
+        // order n = s + 1 folds shifts 0..s
+        mix ^= (uint64_t)V[s] * (uint64_t)ml[s];
+        const OffsetBinary u = offset_binary(mix);
+        const int h0 = (s - 1) * hpn;
+#pragma unroll 4
+        for (int j = 0; j < hpn; ++j) {
+            const int h = h0 + j;
+            srow[h] = kFast ? row_fast(u, hf[h], ho[h]) : row_general(u, hf[h], ho[h], he[h]);
+        }
+    }
+}
+
+// Runtime-shape readout of one staged half tile (nsub tokens x H int64, row
+// pitch `pitch`): one element per lane per step in global order, incremental
+// (row, column).  An int32 destination receives each row id's low 32 bits.
+template <typename OutT>
+__device__ __forceinline__ void readout_runtime(const int64_t* __restrict__ stage,
+                                                OutT* __restrict__ dst, int lane, int nsub,
+                                                int H, int pitch) {
+    const int dq = 32 / H;
+    const int dr = 32 % H;
+    int qq = lane / H;
+    int rr = lane % H;
+    const int nel = nsub * H;
+    for (int e = lane; e < nel; e += 32) {
+        if constexpr (sizeof(OutT) == 8)
+            __stcs(reinterpret_cast<long long*>(dst) + e, (long long)stage[qq * pitch + rr]);
+        else
+            __stcs(reinterpret_cast<int*>(dst) + e, (int)stage[qq * pitch + rr]);
+        rr += dr;
+        qq += dq;
+        if (rr >= H) {
+            rr -= H;
+            ++qq;
+        }
+    }
+}
+
+using KernelFn = void (*)(const RowIdsParams);
+
+// Launch with programmatic stream serialization: the blocks may become
+// resident while the previous kernel in the stream (typically the token-index
+// build) drains; the kernel waits for it before reading anything.
+inline cudaError_t launch_fn(KernelFn fn, const RowIdsParams& p, const RowIdsLaunch& cfg,
+                             cudaStream_t stream) {
+    if (cfg.smem_bytes > 48 * 1024) {
+        // Opting in to more than 48 KB of dynamic shared memory is a function
+        // attribute; setting it is idempotent and not a stream operation.
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.smem_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = cfg.grid;
+    lc.blockDim = cfg.block;
+    lc.dynamicSmemBytes = cfg.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&lc, fn, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace ple

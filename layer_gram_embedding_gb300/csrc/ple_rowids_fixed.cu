@@ -1,0 +1,277 @@
+// The PLE n-gram row-id hash on sm_103a: the fixed-shape kernel.
+//
+// Compiled for the PLE configurations this library is tuned for -- (ngram
+// size, heads per order) in {(3,2), (3,4), (4,4), (5,8)}, each with int32 or
+// int64 ids, int64 or int32 row ids, with or without the context carry.
+// Each lane hashes two tokens of the 64-token tile (lane and lane + 32) per
+// shared constant load; the fast path stages 32-bit remainders as head pairs
+// in rows of odd pitch (8-byte stores hit 16 distinct bank pairs per half
+// warp), and the readout walks the tile in global order ([L, T, H]), adds
+// each head's offset in registers and stores 16 bytes per lane, so a warp
+// store covers 512 consecutive bytes.  Heads off the 32-bit fast path (vocab
+// outside (0, 2^29]) stage int64 rows and read them out 8 bytes at a time.
+#include "ple_rowids_common.cuh"
+
+namespace ple {
+namespace {
+
+__host__ __device__ constexpr int gcd_const(int a, int b) { return b == 0 ? a : gcd_const(b, a % b); }
+
+// Fixed shapes with an even number of heads per order (the PLE
+// configurations this library is tuned for).  Each lane hashes two tokens of
+// the 64-token tile (lane and lane + 32) per constant load; the fast path
+// stages 32-bit remainders as pairs of heads, and the readout adds the head
+// offsets in registers and stores 16 bytes per lane in global order.
+template <int K, int P2, int NC, int GSTEP, bool kVec, bool kFull>
+__device__ __forceinline__ void readout_pairs(const uint2* __restrict__ st,
+                                              long long* __restrict__ dst, int lane, int nsub,
+                                              const int (&soff)[K], const int (&stok)[K],
+                                              const longlong2 (&offs)[NC]) {
+    longlong2* d2 = reinterpret_cast<longlong2*>(dst);
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        if (kFull || stok[j] < nsub) {
+            const uint2 r = st[soff[j]];
+            const longlong2 o = offs[((32 * j) % K) / GSTEP];
+            const longlong2 rows = make_longlong2((long long)((unsigned long long)o.x + r.x),
+                                                  (long long)((unsigned long long)o.y + r.y));
+            if (kVec) {
+                __stcs(d2 + 32 * j + lane, rows);
+            } else {
+                long long* d1 = reinterpret_cast<long long*>(d2 + 32 * j + lane);
+                __stcs(d1, rows.x);
+                __stcs(d1 + 1, rows.y);
+            }
+        }
+    }
+}
+
+// int32 row ids: four heads (two staged pairs) per 16-byte lane store; the
+// offsets' low words are added in 32-bit arithmetic (the low 32 bits of the
+// int64 row id).  K2 quads per token.
+template <int K2, int P2, int NC, int GSTEP, bool kVec, bool kFull>
+__device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int* __restrict__ dst,
+                                              int lane, int nsub, const int (&soff)[K2],
+                                              const int (&stok)[K2], const int4 (&offs)[NC]) {
+    int4* d4 = reinterpret_cast<int4*>(dst);
+#pragma unroll
+    for (int j = 0; j < K2; ++j) {
+        if (kFull || stok[j] < nsub) {
+            const uint2 a = st[soff[j]];
+            const uint2 b = st[soff[j] + 1];
+            const int4 o = offs[((32 * j) % K2) / GSTEP];
+            const int4 rows = make_int4((int)((unsigned)o.x + a.x), (int)((unsigned)o.y + a.y),
+                                        (int)((unsigned)o.z + b.x), (int)((unsigned)o.w + b.y));
+            if (kVec) {
+                __stcs(d4 + 32 * j + lane, rows);
+            } else {
+                int* d1 = reinterpret_cast<int*>(d4 + 32 * j + lane);
+                __stcs(d1, rows.x);
+                __stcs(d1 + 1, rows.y);
+                __stcs(d1 + 2, rows.z);
+                __stcs(d1 + 3, rows.w);
+            }
+        }
+    }
+}
+
+template <typename IdT, int NT, int HPT, typename OutT, bool kCarry>
+__global__ void __launch_bounds__(kMaxWarps * 32)
+row_ids_fixed_kernel(const RowIdsParams p) {
+    static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
+    constexpr int N = NT;
+    constexpr int H = (NT - 1) * HPT;
+    constexpr int K = H / 2;        // 16-byte output chunks (head pairs) per token
+    constexpr int P2 = K | 1;       // staging row pitch in 8-byte pairs (odd)
+    constexpr int PG = H | 1;       // int64 staging pitch for the general path (odd)
+    static_assert(K <= 32, "readout walk assumes K <= 32");
+    const int G = p.group_layers;
+    const int l0 = blockIdx.y * G;
+    const int gl = min(G, p.L - l0);
+    const int nwarps = blockDim.x >> 5;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    wait_prior_grid();
+    if constexpr (kCarry) carry_empty_requests<IdT>(p, N);
+    const SmemLayout sm = carve_smem(smem, G, H, N, nwarps);
+    const int fast_vote = load_group_constants(p, sm, l0, gl, H, N);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTileTokens;
+    const int ntile = (int)max((int64_t)0, min((int64_t)kTileTokens, p.T - t0));
+    int64_t* ids_s = sm.ids + warp * (kHaloSlots + kTileTokens) + kHaloSlots;
+    unsigned char* stage = sm.stage + (size_t)warp * stage_bytes(H, true);
+    const int nA = min(32, ntile);
+    const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
+    int64_t VA[N], VB[N];
+    if (ntile > 0) {
+        stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+        int32_t rA, qA, rB, qB;
+        window<IdT, N, N, false>(p, ids_s, t0, lane, lane < nA, N, VA, rA, qA);
+        window<IdT, N, N, false>(p, ids_s, t0, 32 + lane, lane < nB, N, VB, rB, qB);
+        if (kCarry && blockIdx.y == 0) {
+            carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
+            carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
+        }
+    }
+    const bool all_fast = __syncthreads_and(fast_vote) != 0;
+    if (ntile == 0) return;
+
+    if (!all_fast) {
+        // some head of this group is off the fast path: int64 rows, 8-byte
+        // readout, one half tile at a time
+        int64_t* st = reinterpret_cast<int64_t*>(stage);
+#pragma unroll 1
+        for (int u = 0; u < 2; ++u) {
+            const int nsub = u == 0 ? nA : nB;
+            if (nsub <= 0) break;
+#pragma unroll 1
+            for (int l = 0; l < gl; ++l) {
+                const int hb = l * H;
+                hash_layer<N, N, false>(u == 0 ? VA : VB, N, HPT, sm.mul + l * N, sm.fast + hb,
+                                        sm.off + hb, sm.ext + hb, st + lane * PG);
+                __syncwarp();
+                OutT* dst = static_cast<OutT*>(p.out) +
+                            ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
+                readout_runtime<OutT>(st, dst, lane, nsub, H, PG);
+                __syncwarp();
+            }
+        }
+        return;
+    }
+
+    const uint2* stA = reinterpret_cast<const uint2*>(stage);
+    uint2* stAw = reinterpret_cast<uint2*>(stage);
+    // readout walk, the same for every layer: a 16-byte store carries U staged
+    // pairs (1 for int64, 2 for int32), KU such units per token; unit c =
+    // 32 j + lane of a half tile is token c / KU, column c % KU; with
+    // q0 = lane / KU, r0 = lane % KU the step j adds the compile-time
+    // (32 j) / KU and (32 j) % KU, carrying one token when the column wraps
+    constexpr int U = sizeof(OutT) == 8 ? 1 : 2;
+    static_assert(K % U == 0, "int32 output needs a multiple of 4 heads");
+    constexpr int KU = K / U;
+    constexpr int GU = gcd_const(32, KU);
+    constexpr int NU = KU / GU;
+    const int q0 = lane / KU;
+    const int r0 = lane % KU;
+    int soff[KU], stok[KU];
+#pragma unroll
+    for (int j = 0; j < KU; ++j) {
+        const int cj = (32 * j) % KU;
+        const bool carry = r0 + cj >= KU;
+        stok[j] = q0 + (32 * j) / KU + (carry ? 1 : 0);
+        soff[j] = stok[j] * P2 + U * (r0 + cj - (carry ? KU : 0));
+    }
+    const bool full = nA == 32 && nB == 32;
+    const bool vec_out = p.out_vec_ok != 0;
+
+#pragma unroll 1
+    for (int l = 0; l < gl; ++l) {
+        const int64_t* ml = sm.mul + l * N;
+        const uint4* hf = sm.fast + l * H;
+        uint64_t mixA = (uint64_t)VA[0] * (uint64_t)ml[0];
+        uint64_t mixB = (uint64_t)VB[0] * (uint64_t)ml[0];
+#pragma unroll
+        for (int s = 1; s < N; ++s) {
+            const uint64_t m = (uint64_t)ml[s];
+            mixA ^= (uint64_t)VA[s] * m;
+            mixB ^= (uint64_t)VB[s] * m;
+            const OffsetBinary uA = offset_binary(mixA);
+            const OffsetBinary uB = offset_binary(mixB);
+#pragma unroll
+            for (int j = 0; j < HPT; j += 2) {
+                const int h = (s - 1) * HPT + j;
+                const uint4 c0 = hf[h];
+                const uint4 c1 = hf[h + 1];
+                stAw[lane * P2 + h / 2] = make_uint2(floormod_fast(uA, c0), floormod_fast(uA, c1));
+                stAw[(32 + lane) * P2 + h / 2] =
+                    make_uint2(floormod_fast(uB, c0), floormod_fast(uB, c1));
+            }
+        }
+        __syncwarp();
+        OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
+        if constexpr (U == 1) {
+            // this lane's readout columns' offsets for layer l
+            longlong2 offs[NU];
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
+            }
+            long long* d = reinterpret_cast<long long*>(dst);
+            if (full && vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                         soff, stok, offs);
+            } else if (vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                              nB, soff, stok, offs);
+            } else {
+                readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                               nB, soff, stok, offs);
+            }
+        } else {
+            int4 offs[NU];
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                const int64_t* o = sm.off + l * H + 4 * col;
+                offs[k] = make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]);
+            }
+            int* d = reinterpret_cast<int*>(dst);
+            if (full && vec_out) {
+                readout_quads<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                readout_quads<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                         soff, stok, offs);
+            } else if (vec_out) {
+                readout_quads<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quads<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                              nB, soff, stok, offs);
+            } else {
+                readout_quads<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quads<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                               nB, soff, stok, offs);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <typename IdT, typename OutT, bool kCarry>
+KernelFn pick_fixed(int N, int hpn) {
+    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT, kCarry>;
+    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT, kCarry>;
+    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT, kCarry>;
+    return row_ids_fixed_kernel<IdT, 5, 8, OutT, kCarry>;
+}
+
+template <typename IdT, typename OutT>
+KernelFn pick_fixed(int N, int hpn, bool carry) {
+    return carry ? pick_fixed<IdT, OutT, true>(N, hpn) : pick_fixed<IdT, OutT, false>(N, hpn);
+}
+
+}  // namespace
+
+cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                                 cudaStream_t stream) {
+    const bool carry = p.next_ctx != nullptr;
+    KernelFn fn;
+    if (p.out_bytes == 4)
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int32_t>(p.N, p.hpn, carry)
+                           : pick_fixed<int64_t, int32_t>(p.N, p.hpn, carry);
+    else
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int64_t>(p.N, p.hpn, carry)
+                           : pick_fixed<int64_t, int64_t>(p.N, p.hpn, carry);
+    return launch_fn(fn, p, cfg, stream);
+}
+
+}  // namespace ple

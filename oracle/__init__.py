@@ -65,6 +65,8 @@ def _load():
             lib.oracle_floor_mod.restype = i64
             lib.oracle_token_index.argtypes = [p, i32, i64, c_int, p, p]
             lib.oracle_token_index.restype = c_int
+            lib.oracle_next_context.argtypes = [p, c_int, i64, p, p, p, i32, i32, p]
+            lib.oracle_next_context.restype = c_int
             rargs = [p, c_int, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, i64, p]
             for name in ("oracle_row_ids", "oracle_row_ids_reading_b"):
                 fn = getattr(lib, name)
@@ -95,6 +97,22 @@ def token_index(cu_seqlens, num_requests: int, num_tokens: int, is_decode: bool)
     if rc != ORC_OK:
         raise OracleError(rc, "oracle_token_index")
     return req, local
+
+
+def next_context(input_ids, req, local, ngram_context):
+    """Each request's context for its next call: the last ctx_len ids of its
+    context row followed by its tokens of this batch ([B, ctx_len])."""
+    ids = np.ascontiguousarray(input_ids)
+    ctx = np.ascontiguousarray(ngram_context, dtype=ids.dtype)
+    req = np.ascontiguousarray(req, dtype=np.int32)
+    local = np.ascontiguousarray(local, dtype=np.int32)
+    out = np.zeros_like(ctx)
+    rc = _load().oracle_next_context(_ptr(ids), ids.dtype.itemsize, ids.shape[0], _ptr(req),
+                                     _ptr(local), _ptr(ctx), ctx.shape[0], ctx.shape[1],
+                                     _ptr(out))
+    if rc != ORC_OK:
+        raise OracleError(rc, "oracle_next_context")
+    return out
 
 
 def row_ids(input_ids, req, local, ngram_context, layer_multipliers, vocab_sizes, offsets,

@@ -216,6 +216,54 @@ done:
     return rc;
 }
 
+/* The context each request carries into its next call: the last ctx_len ids
+ * of (its ngram_context row, then its tokens of this batch), oldest first
+ * ("What", second observation: ngram_context holds each request's ids just
+ * before the batch).  A request with no token in the batch keeps its row.
+ * (req, local) must describe a packed batch, as for oracle_row_ids. */
+int oracle_next_context(const void* input_ids, int id_bytes, int64_t T, const int32_t* req,
+                        const int32_t* local, const void* ngram_context, int32_t B,
+                        int32_t ctx_len, void* next_context) {
+    if (T < 0 || B < 1 || ctx_len < 0 || (id_bytes != 4 && id_bytes != 8)) return ORC_ERR_ARG;
+    if (!ngram_context || !next_context || (T > 0 && (!input_ids || !req || !local)))
+        return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    int64_t* len = (int64_t*)malloc(sizeof(int64_t) * (size_t)B);
+    int64_t* start = (int64_t*)malloc(sizeof(int64_t) * (size_t)B);
+    int64_t* seq = NULL;
+    if (!len || !start) {
+        rc = ORC_ERR_ALLOC;
+        goto done;
+    }
+    rc = check_index(req, local, T, B, len, start);
+    if (rc != ORC_OK) goto done;
+    for (int32_t r = 0; r < B; ++r) {
+        /* the request's whole known history: context row, then its tokens */
+        const int64_t n = (int64_t)ctx_len + len[r];
+        free(seq);
+        seq = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+        if (!seq) {
+            rc = ORC_ERR_ALLOC;
+            goto done;
+        }
+        for (int32_t c = 0; c < ctx_len; ++c)
+            seq[c] = load_id(ngram_context, id_bytes, (int64_t)r * ctx_len + c);
+        for (int64_t i = 0; i < len[r]; ++i) seq[ctx_len + i] = load_id(input_ids, id_bytes, start[r] + i);
+        for (int32_t c = 0; c < ctx_len; ++c) {
+            const int64_t v = seq[n - ctx_len + c];
+            if (id_bytes == 4)
+                ((int32_t*)next_context)[(int64_t)r * ctx_len + c] = (int32_t)v;
+            else
+                ((int64_t*)next_context)[(int64_t)r * ctx_len + c] = v;
+        }
+    }
+done:
+    free(len);
+    free(start);
+    free(seq);
+    return rc;
+}
+
 /* Row ids under reading A (an invalid shift hashes the boundary id).
  * Arguments mean what they mean for the CUDA library's ple_row_ids; every
  * pointer is a host pointer.  out is [L, T, H] int64. */

@@ -152,6 +152,100 @@ def test_int32_row_ids_decode_without_index():
     assert_same(out, low32(oracle_rows(batch)), "int32 decode")
 
 
+def gpu_rows_carry(batch, out_dtype=torch.int64, index_free=False):
+    ctx = dev(batch.ngram_context)
+    nxt = torch.full_like(ctx, -5)
+    if index_free:
+        req = local = cu = None
+    else:
+        req, local = gpu_index(batch)
+        cu = dev(batch.cu_seqlens) if batch.cu_seqlens is not None else dev(
+            np.arange(batch.num_requests + 1, dtype=np.int32))
+    out = ple.ple_row_ids(dev(batch.ids), req, local, ctx, dev(batch.layer_multipliers),
+                          dev(batch.vocab_sizes), dev(batch.offsets), batch.ngram_size,
+                          batch.heads_per_ngram, batch.boundary_id, out_dtype=out_dtype,
+                          cu_seqlens=cu, next_context=nxt)
+    return out, nxt
+
+
+def oracle_carry(batch):
+    req, local = oracle_index(batch)
+    return oracle.next_context(batch.ids, req, local, batch.ngram_context)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_context_carry_full_size(name):
+    """ple_row_ids_ex: the same row ids, plus every request's carried context."""
+    batch = WORKLOADS[name]
+    out, nxt = gpu_rows_carry(batch)
+    assert_same(out, oracle_rows(batch), f"{name} rows with carry")
+    assert_same(nxt, oracle_carry(batch), f"{name} carried context")
+    if batch.is_decode:
+        out, nxt = gpu_rows_carry(batch, index_free=True)
+        assert_same(out, oracle_rows(batch), f"{name} rows, index-free carry")
+        assert_same(nxt, oracle_carry(batch), f"{name} carried context, index-free")
+
+
+@pytest.mark.parametrize("chunk", range(3))
+def test_context_carry_random_edges(chunk):
+    """Empty requests keep their row, short requests mix context and tokens,
+    int32 ids and int32 row ids."""
+    for seed in range(chunk * 50, (chunk + 1) * 50):
+        batch = wl.random_batch(11000 + seed, T_max=120,
+                                ids_dtype=np.int32 if seed % 2 else np.int64)
+        out_dtype = torch.int32 if seed % 3 == 0 else torch.int64
+        out, nxt = gpu_rows_carry(batch, out_dtype=out_dtype)
+        exp = oracle_rows(batch)
+        assert_same(out, low32(exp) if out_dtype == torch.int32 else exp, f"carry rows {seed}")
+        assert_same(nxt, oracle_carry(batch), f"carried context {seed}")
+
+
+def test_decode_steps_chain_through_the_carry():
+    """Five decode steps, each fed the context the previous step carried,
+    against the oracle run step by step."""
+    b = wl.decode(8)
+    ctx_o = b.ngram_context.copy()
+    ctx_g = dev(b.ngram_context)
+    M, vocab, off = dev(b.layer_multipliers), dev(b.vocab_sizes), dev(b.offsets)
+    for step in range(5):
+        ids = wl.decode(8, 10 + step).ids
+        nxt = torch.empty_like(ctx_g)
+        out = ple.ple_row_ids(dev(ids), None, None, ctx_g, M, vocab, off, 3, 2, b.boundary_id,
+                              next_context=nxt)
+        sb = dataclasses.replace(b, ids=ids, ngram_context=ctx_o)
+        assert_same(out, oracle_rows(sb), f"decode step {step}")
+        ctx_o = oracle_carry(sb)
+        assert_same(nxt, ctx_o, f"carry after step {step}")
+        ctx_g = nxt
+
+
+def test_chunked_prefill_through_the_carry_equals_one_prefill():
+    """The first request of the large prefill hashed in four chunks, each
+    chunk using the context the GPU carried out of the previous one, gives
+    the rows of one prefill."""
+    full = wl.prefill_262144()
+    start = int(full.cu_seqlens[1])  # the first request's length
+    first = wl.Batch("r0", full.ids[:start], full.ngram_context[:1],
+                     np.array([0, start], np.int32), False, full.layer_multipliers,
+                     full.vocab_sizes, full.offsets, 4, 4)
+    whole = oracle_rows(first)
+    ctx = dev(first.ngram_context)
+    cuts = [0, 1, 37, start // 2, start]
+    parts = []
+    for a, c in zip(cuts[:-1], cuts[1:]):
+        chunk = dataclasses.replace(first, ids=first.ids[a:c],
+                                    cu_seqlens=np.array([0, c - a], np.int32))
+        nxt = torch.empty_like(ctx)
+        req, local = ple.ple_build_token_index(dev(chunk.cu_seqlens), 1, c - a, False)
+        parts.append(ple.ple_row_ids(dev(chunk.ids), req, local, ctx,
+                                     dev(chunk.layer_multipliers), dev(chunk.vocab_sizes),
+                                     dev(chunk.offsets), 4, 4, chunk.boundary_id,
+                                     cu_seqlens=dev(chunk.cu_seqlens), next_context=nxt))
+        ctx = nxt
+    got = torch.cat(parts, dim=1)
+    assert_same(got, whole, "chunked prefill through the carry")
+
+
 @pytest.mark.parametrize("chunk", range(6))
 def test_random_edge_batches(chunk):
     """Small ragged batches spanning several 64-token tiles with ragged tails,

@@ -100,6 +100,31 @@ def test_row_ids_host_checks(lib, kw, status):
     assert row_ids(lib, **kw) == status
 
 
+def row_ids_ex(lib, **kw):
+    a = dict(ids=A, dtype=1, T=64, req=A, local=A, ctx=A, B=1, ctx_len=2, M=A, vocab=A, off=A,
+             H=4, N=3, hpn=2, L=1, b=7, out=A, out_dtype=1, cu=A, nxt=A)
+    a.update(kw)
+    return lib.ple_row_ids_ex(a["ids"], a["dtype"], a["T"], a["req"], a["local"], a["ctx"],
+                              a["B"], a["ctx_len"], a["M"], a["vocab"], a["off"], a["H"], a["N"],
+                              a["hpn"], a["L"], a["b"], a["out"], a["out_dtype"], a["cu"],
+                              a["nxt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(out_dtype=2), ple.PLE_ERR_DTYPE),
+    (dict(out_dtype=2, ctx_len=1), ple.PLE_ERR_GEOMETRY_CTX),   # geometry first
+    (dict(out_dtype=-1, T=0), ple.PLE_ERR_DTYPE),
+    (dict(cu=None), ple.PLE_ERR_NULL),                          # carry needs cu_seqlens
+    (dict(nxt=A + 4), ple.PLE_ERR_ALIGN),
+    (dict(cu=A + 2), ple.PLE_ERR_ALIGN),
+    (dict(out_dtype=0, out=A + 2), ple.PLE_ERR_ALIGN),
+    (dict(out_dtype=1, out=A + 4), ple.PLE_ERR_ALIGN),
+    (dict(req=None, local=None, cu=None, T=4, B=5), ple.PLE_ERR_SIZE),
+])
+def test_row_ids_ex_host_checks(lib, kw, status):
+    assert row_ids_ex(lib, **kw) == status
+
+
 def test_row_ids_empty_batch_is_ok_without_pointers(lib):
     assert row_ids(lib, T=0, ids=None, req=None, local=None, ctx=None, M=None, vocab=None,
                    off=None, out=None, B=0) == ple.PLE_OK

@@ -280,6 +280,51 @@ def test_int32_ids_equal_int64_ids():
 
 
 # --------------------------------------------------------------------------
+# the carried context
+
+
+def test_next_context_is_the_tail_of_context_and_tokens():
+    """Definition, written out with numpy: last N-1 of (context row, tokens)."""
+    for seed in range(200):
+        batch = wl.random_batch(seed, T_max=30)
+        req, local = oracle.token_index(batch.cu_seqlens, batch.num_requests, batch.num_tokens,
+                                        batch.is_decode)
+        got = oracle.next_context(batch.ids, req, local, batch.ngram_context)
+        C = batch.ngram_size - 1
+        for r in range(batch.num_requests):
+            toks = batch.ids[req == r]
+            hist = np.concatenate([batch.ngram_context[r], toks])
+            assert np.array_equal(got[r], hist[len(hist) - C:]), (seed, r)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_carried_context_chains_chunks(seed):
+    """I4 through the oracle's own carry: hashing a request in chunks, each
+    chunk with the context the previous chunk carried, equals one prefill."""
+    full = wl.random_batch(3000 + seed, decode_batch=False, T_max=60)
+    lengths = np.diff(full.cu_seqlens)
+    r = int(np.argmax(lengths))
+    T0 = int(lengths[r])
+    start = int(full.cu_seqlens[r])
+    ids = full.ids[start:start + T0]
+    one = wl.Batch("one", ids, full.ngram_context[r:r + 1], np.array([0, T0], np.int32), False,
+                   full.layer_multipliers, full.vocab_sizes, full.offsets, full.ngram_size,
+                   full.heads_per_ngram, full.boundary_id)
+    rng = np.random.default_rng(seed)
+    cuts = np.unique(np.concatenate([[0, T0], rng.integers(0, T0 + 1, size=3)]))
+    ctx = full.ngram_context[r:r + 1]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        chunk = wl.Batch("c", ids[a:b], ctx, np.array([0, b - a], np.int32), False,
+                         full.layer_multipliers, full.vocab_sizes, full.offsets,
+                         full.ngram_size, full.heads_per_ngram, full.boundary_id)
+        parts.append(run_oracle(chunk))
+        req, local = oracle.token_index(chunk.cu_seqlens, 1, chunk.num_tokens, False)
+        ctx = oracle.next_context(chunk.ids, req, local, ctx)
+    assert np.array_equal(np.concatenate(parts, axis=1), run_oracle(one))
+
+
+# --------------------------------------------------------------------------
 # geometry preconditions ("Why it is safe", last point) and domain errors
 
 
