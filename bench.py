@@ -50,7 +50,7 @@ METRIC = "row-ids/sec and % HBM roofline at large prefill; device µs/call at de
 UNIT = "row-ids/s"
 L2_BYTES = 126 * 2 ** 20
 ROTATE = 64
-KERNEL_SOURCES = ["ple_row_ids.cu", "ple_divmod.cuh", "ple_internal.h"]
+KERNEL_SOURCES = ["ple_rowids_common.cuh", "ple_rowids_fixed.cu", "ple_divmod.cuh", "ple_internal.h"]
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "row_ids_prefill_262144_traffic.json")
 
 

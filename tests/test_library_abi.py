@@ -181,3 +181,8 @@ def test_library_has_no_host_compute_path():
     for f in os.listdir(ora):
         if f.endswith((".py", ".c")):
             assert "layer_gram_embedding_gb300" not in open(os.path.join(ora, f)).read()
+
+
+def test_bench_kernel_source_list_exists():
+    import bench
+    assert len(bench.kernel_source_hash()) == 16
