@@ -68,6 +68,8 @@ def _load():
             lib.oracle_next_context.argtypes = [p, c_int, i64, p, p, p, i32, i32, p]
             lib.oracle_next_context.restype = c_int
             rargs = [p, c_int, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, i64, p]
+            lib.oracle_row_embed.argtypes = rargs[:-1] + [p, i64, i32, p, p]
+            lib.oracle_row_embed.restype = c_int
             for name in ("oracle_row_ids", "oracle_row_ids_reading_b"):
                 fn = getattr(lib, name)
                 fn.argtypes = rargs
@@ -158,3 +160,32 @@ def row_ids(input_ids, req, local, ngram_context, layer_multipliers, vocab_sizes
     if rc != ORC_OK:
         raise OracleError(rc, "oracle_row_ids")
     return out
+
+
+def row_embed(input_ids, req, local, ngram_context, layer_multipliers, vocab_sizes, offsets,
+              ngram_size: int, heads_per_ngram: int, boundary_id: int, table):
+    """(emb, abs_sum), both [L, T, D] float64: the sum over heads of the rows
+    of `table` ([L, V, D] bfloat16 bits as uint16) that the row ids name,
+    and the sum of their absolute values (for an accumulation error bound).
+    Row ids outside [0, V) add nothing."""
+    ids = np.ascontiguousarray(input_ids)
+    ctx = np.ascontiguousarray(ngram_context, dtype=ids.dtype)
+    req = np.ascontiguousarray(req, dtype=np.int32)
+    local = np.ascontiguousarray(local, dtype=np.int32)
+    M = np.ascontiguousarray(layer_multipliers, dtype=np.int64).reshape(-1, int(ngram_size))
+    L = M.shape[0]
+    vocab = np.ascontiguousarray(vocab_sizes, dtype=np.int64).reshape(L, -1)
+    off = np.ascontiguousarray(offsets, dtype=np.int64).reshape(L, -1)
+    tab = np.ascontiguousarray(table, dtype=np.uint16)
+    if tab.ndim != 3 or tab.shape[0] != L:
+        raise ValueError("table must be [L, V, D]")
+    T, H, V, D = ids.shape[0], vocab.shape[1], tab.shape[1], tab.shape[2]
+    out = np.zeros((L, T, D), dtype=np.float64)
+    abs_sum = np.zeros((L, T, D), dtype=np.float64)
+    rc = _load().oracle_row_embed(_ptr(ids), ids.dtype.itemsize, T, _ptr(req), _ptr(local),
+                                  _ptr(ctx), ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab),
+                                  _ptr(off), H, int(ngram_size), int(heads_per_ngram), L,
+                                  int(boundary_id), _ptr(tab), V, D, _ptr(out), _ptr(abs_sum))
+    if rc != ORC_OK:
+        raise OracleError(rc, "oracle_row_embed")
+    return out, abs_sum

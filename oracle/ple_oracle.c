@@ -264,6 +264,55 @@ done:
     return rc;
 }
 
+/* bfloat16 bits to a double: the bits are the top half of an IEEE float. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* The consumer of the row ids ("What": the ids are table row ids): for each
+ * layer l and token t, the sum over heads of the table rows they name,
+ *   emb[l][t][:] = sum_h table[l][row(l,t,h)][:],
+ * with table [L, V, D] bfloat16 bits; a row id outside [0, V) adds nothing.
+ * The sum is taken in double (exact for these inputs); abs_sum receives
+ * sum_h |table[l][row][:]| for the floating-point error bound of a float
+ * accumulation.  out and abs_sum are [L, T, D] doubles. */
+int oracle_row_embed(const void* input_ids, int id_bytes, int64_t T, const int32_t* req,
+                     const int32_t* local, const void* ngram_context, int32_t B, int32_t ctx_len,
+                     const int64_t* M, const int64_t* vocab, const int64_t* off, int32_t H,
+                     int32_t N, int32_t hpn, int32_t L, int64_t b, const uint16_t* table,
+                     int64_t V, int32_t D, double* out, double* abs_sum) {
+    if (V < 0 || D < 1 || (T > 0 && (!table || !out || !abs_sum))) return ORC_ERR_ARG;
+    if (T == 0) return ORC_OK;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(L * T * H));
+    if (!rows) return ORC_ERR_ALLOC;
+    int rc = row_ids_impl(input_ids, id_bytes, T, req, local, ngram_context, B, ctx_len, M, vocab,
+                          off, H, N, hpn, L, b, 0, rows);
+    if (rc == ORC_OK) {
+        for (int32_t l = 0; l < L; ++l) {
+            for (int64_t t = 0; t < T; ++t) {
+                double* o = out + ((int64_t)l * T + t) * D;
+                double* a = abs_sum + ((int64_t)l * T + t) * D;
+                for (int32_t d = 0; d < D; ++d) o[d] = a[d] = 0.0;
+                for (int32_t h = 0; h < H; ++h) {
+                    const int64_t row = rows[((int64_t)l * T + t) * H + h];
+                    if (row < 0 || row >= V) continue;
+                    const uint16_t* e = table + ((int64_t)l * V + row) * D;
+                    for (int32_t d = 0; d < D; ++d) {
+                        const double x = bf16_to_double(e[d]);
+                        o[d] += x;
+                        a[d] += x < 0 ? -x : x;
+                    }
+                }
+            }
+        }
+    }
+    free(rows);
+    return rc;
+}
+
 /* Row ids under reading A (an invalid shift hashes the boundary id).
  * Arguments mean what they mean for the CUDA library's ple_row_ids; every
  * pointer is a host pointer.  out is [L, T, H] int64. */

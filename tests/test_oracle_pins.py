@@ -325,6 +325,72 @@ def test_carried_context_chains_chunks(seed):
 
 
 # --------------------------------------------------------------------------
+# the table gather (the row ids' consumer)
+
+
+def oracle_embed(batch, table):
+    req, local = oracle.token_index(batch.cu_seqlens, batch.num_requests, batch.num_tokens,
+                                    batch.is_decode)
+    return oracle.row_embed(batch.ids, req, local, batch.ngram_context, batch.layer_multipliers,
+                            batch.vocab_sizes, batch.offsets, batch.ngram_size,
+                            batch.heads_per_ngram, batch.boundary_id, table)
+
+
+def test_embed_worked_example():
+    g = json.load(open(GOLDEN))
+    batch = golden_batch(g["setup"])
+    V, D = g["embed"]["table_rows"], g["embed"]["dim"]
+    vals = np.stack([np.arange(V), -2 * np.arange(V)], axis=1).astype(np.float32)
+    table = wl.bf16_bits(vals).reshape(1, V, D)
+    emb, _ = oracle_embed(batch, table)
+    assert emb.tolist() == g["embed"]["expected"]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_embed_of_a_row_valued_table_is_the_sum_of_row_ids(seed):
+    """Row r of the table holds the value r (exact in bfloat16 below 256):
+    the gathered sum is the sum of the (pinned) row ids over heads."""
+    batch, _ = wl.small_table_batch(seed, D=3, T_max=40)
+    rng = np.random.default_rng(seed)
+    H = batch.num_heads
+    batch.vocab_sizes[:] = rng.integers(1, max(2, 255 // H), size=batch.vocab_sizes.shape)
+    batch.offsets[:] = wl.prefix_offsets(batch.vocab_sizes)
+    V = int(batch.vocab_sizes.sum(axis=1).max())
+    vals = np.repeat(np.arange(V, dtype=np.float32)[:, None], 3, axis=1)
+    table = np.broadcast_to(wl.bf16_bits(vals), (batch.num_layers, V, 3)).copy()
+    emb, _ = oracle_embed(batch, table)
+    rows = run_oracle(batch)
+    assert np.array_equal(emb[..., 0], rows.sum(axis=2).astype(np.float64))
+    assert np.array_equal(emb[..., 1], emb[..., 0]) and np.array_equal(emb[..., 2], emb[..., 0])
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_embed_of_a_one_hot_table_counts_heads_per_row(seed):
+    batch, _ = wl.small_table_batch(seed, T_max=30, L=2)
+    batch.vocab_sizes[:] = np.minimum(batch.vocab_sizes, 17)
+    batch.offsets[:] = wl.prefix_offsets(batch.vocab_sizes)
+    V = int(batch.vocab_sizes.sum(axis=1).max())
+    table = np.broadcast_to(wl.bf16_bits(np.eye(V, dtype=np.float32)),
+                            (batch.num_layers, V, V)).copy()
+    emb, _ = oracle_embed(batch, table)
+    rows = run_oracle(batch)
+    for l in range(batch.num_layers):
+        for t in range(batch.num_tokens):
+            counts = np.bincount(rows[l, t], minlength=V)[:V]
+            assert np.array_equal(emb[l, t], counts.astype(np.float64))
+
+
+def test_embed_rows_outside_the_table_add_nothing():
+    batch, table = wl.small_table_batch(5, D=8, T_max=60)
+    V = table.shape[1]
+    cut = V // 2
+    full, _ = oracle_embed(batch, np.concatenate(
+        [table[:, :cut], np.zeros_like(table[:, cut:])], axis=1))
+    short, _ = oracle_embed(batch, table[:, :cut])
+    assert np.array_equal(full, short)
+
+
+# --------------------------------------------------------------------------
 # geometry preconditions ("Why it is safe", last point) and domain errors
 
 

@@ -328,3 +328,32 @@ def slice_batch(batch: Batch, start: int, stop: int) -> Batch:
     ctx = np.stack(ctx_rows).astype(batch.ngram_context.dtype)
     return replace(batch, name=f"{batch.name}[{start}:{stop}]", ids=batch.ids[start:stop],
                    ngram_context=ctx, cu_seqlens=cu_from_lengths(lengths))
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 values to bfloat16 bit patterns (uint16), rounding to nearest
+    even.  Input construction only."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def embed_table(rng: np.random.Generator, L: int, V: int, D: int) -> np.ndarray:
+    """A synthetic per-layer embedding table [L, V, D] of bfloat16 bits with
+    standard-normal values (no trained weights exist for this path)."""
+    return bf16_bits(rng.standard_normal((L, V, D), dtype=np.float32))
+
+
+def small_table_batch(seed: int, D: int = 16, T_max: int = 100, N=None, hpn=None, L=None,
+                      ids_dtype=np.int64, decode_batch=None) -> tuple:
+    """A random batch whose heads index a small table (vocab primes below
+    2^12, prefix-sum offsets), with that table; V is the largest per-layer
+    vocab total, so every row id is in range unless the caller shrinks V."""
+    batch = random_batch(seed, T_max=T_max, N=N, hpn=hpn, L=L, ids_dtype=ids_dtype,
+                         decode_batch=decode_batch)
+    rng = np.random.default_rng(seed + 1)
+    H = batch.num_heads
+    vocab = random_primes(rng, batch.num_layers * H, 2, 2 ** 12).reshape(batch.num_layers, H)
+    batch = replace(batch, vocab_sizes=vocab, offsets=prefix_offsets(vocab))
+    V = int(vocab.sum(axis=1).max())
+    return batch, embed_table(rng, batch.num_layers, V, D)
