@@ -619,6 +619,64 @@ def all_configs(args):
     return 0
 
 
+def embed_bench(args):
+    """The fused table gather on the large-prefill shape: a 256-wide bfloat16
+    table per layer with one row per head vocabulary entry (about 7.1 M rows,
+    29 GB over 8 layers), one JSON line with the gather's HBM rate."""
+    import torch
+
+    import layer_gram_embedding_gb300 as ple
+    from layer_gram_embedding_gb300 import build as lib_build
+
+    lib_build.build()
+    device = torch.device("cuda", 0)
+    b = wl.prefill_262144()
+    T, B, L, H, N = b.num_tokens, b.num_requests, b.num_layers, b.num_heads, b.ngram_size
+    D = args.embed_dim
+    V = int(b.vocab_sizes.sum(axis=1).max())
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4000)
+    table = torch.randn((L, V, D), dtype=torch.bfloat16, device=device, generator=gen)
+    ids, ctx, cu = to_dev(b.ids), to_dev(b.ngram_context), to_dev(b.cu_seqlens)
+    M, vocab, off = to_dev(b.layer_multipliers), to_dev(b.vocab_sizes), to_dev(b.offsets)
+    req, local = ple.ple_build_token_index(cu, B, T, False)
+    out = torch.empty((L, T, D), dtype=torch.float32, device=device)
+
+    def call():
+        ple.ple_row_embed(ids, req, local, ctx, M, vocab, off, N, b.heads_per_ngram,
+                          b.boundary_id, table, out=out)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(device)
+    steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    gather = L * T * H * D * 2
+    written = L * T * D * 4
+    total = gather + written + T * 16 + B * (N - 1) * 8 + 8 * L * (N + 2 * H)
+    peaks, kind = measured_peaks()
+    gbs = total / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "fused PLE table gather (hash + gather, row ids never written)",
+        "workload": f"{b.name}: T={T}, L={L}, H={H}, D={D}, V={V} rows per layer, bf16 table "
+                    f"{L * V * D * 2 / 1e9:.1f} GB, fp32 out",
+        "ms_per_call": ms, "embeddings_per_s": L * T / (ms / 1e3),
+        "algorithmic_bytes": total, "gather_bytes": gather, "out_bytes": written,
+        "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+        "peak_kind": kind, "steps": steps, "launches_per_call": 1}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,6 +688,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of single-thread oracle work for cpu_baseline")
+    ap.add_argument("--embed", action="store_true",
+                    help="time the fused table gather instead of the contract line")
+    ap.add_argument("--embed-dim", type=int, default=256)
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload (graph of 300 calls) instead of the contract line")
     args = ap.parse_args(argv)
@@ -639,6 +700,8 @@ def main(argv=None):
         return reference_arm(args)
     if args.all_configs:
         return all_configs(args)
+    if args.embed:
+        return embed_bench(args)
     return our_arm(args)
 
 

@@ -52,6 +52,7 @@ typedef enum { PLE_I32 = 0, PLE_I64 = 1 } ple_id_dtype;
 
 #define PLE_MAX_NGRAM 16   /* largest supported ngram_size */
 #define PLE_MAX_HEADS 256  /* largest supported heads per layer */
+#define PLE_MAX_EMBED_DIM 65536  /* largest supported table row width */
 
 /*
  * ple_build_token_index -- per-token (request, offset) index.
@@ -198,6 +199,36 @@ ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_t
                           int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
                           int64_t boundary_id, void* out, int32_t out_dtype,
                           const int32_t* cu_seqlens, void* next_context, void* stream);
+
+/*
+ * ple_row_embed -- the row ids' table gather, fused with the hash.
+ *
+ * The row ids of section "What" are table row ids; this call hashes them
+ * exactly as ple_row_ids does and, without writing them, sums over heads the
+ * rows of the layer's embedding table that they name:
+ *   out[l][t][:] = sum over h of table[l][row(l,t,h)][:]
+ * accumulated in fp32 in head order (h = 0 first); a row id outside
+ * [0, table_rows) adds nothing.  One launch for every layer.
+ *
+ *   all arguments up to boundary_id: as ple_row_ids (req = local = NULL is
+ *                 the index-free decode).
+ *   table         [L, table_rows, dim] bfloat16 (as raw 16-bit patterns),
+ *                 device, 16-byte aligned; may be NULL when table_rows == 0.
+ *   table_rows    V >= 0 rows per layer.
+ *   dim           D, a multiple of 8 in [8, PLE_MAX_EMBED_DIM].
+ *   out           [L, T, D] float, device, 16-byte aligned; every element is
+ *                 written.
+ *
+ * Errors: as ple_row_ids, plus PLE_ERR_SIZE for dim / table_rows and
+ * PLE_ERR_ALIGN for a table or out that is not 16-byte aligned.
+ */
+ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                         const int32_t* req, const int32_t* local, const void* ngram_context,
+                         int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
+                         const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
+                         int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
+                         int64_t boundary_id, const void* table, int64_t table_rows, int32_t dim,
+                         float* out, void* stream);
 
 /*
  * ple_selftest_floor_mod -- diagnostic: the library's invariant-divisor

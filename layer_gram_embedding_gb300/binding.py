@@ -32,6 +32,7 @@ PLE_I32 = 0
 PLE_I64 = 1
 PLE_MAX_NGRAM = 16
 PLE_MAX_HEADS = 256
+PLE_MAX_EMBED_DIM = 65536
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libple.so")
 
@@ -45,6 +46,8 @@ SIGNATURES = {
                                _I32, _I32, _I64, _P, _P]),
     "ple_row_ids_ex": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
                               _I32, _I32, _I64, _P, _I32, _P, _P, _P]),
+    "ple_row_embed": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
+                             _I32, _I32, _I64, _P, _I64, _I32, _P, _P]),
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
@@ -244,6 +247,58 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                                       _ptr(cu_seqlens) if cu_seqlens is not None
                                       else ctypes.c_void_p(0), _ptr(next_context),
                                       _stream_handle(stream, dev))
+    _check(st, where)
+    return out
+
+
+def ple_row_embed(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.Tensor | None,
+                  ngram_context: torch.Tensor, layer_multipliers: torch.Tensor,
+                  vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
+                  heads_per_ngram: int, boundary_id: int, table: torch.Tensor,
+                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """[L, T, D] float32: per layer and token, the sum over heads of the rows
+    of `table` ([L, V, D] bfloat16, or its raw 16-bit patterns) that the row
+    ids name -- the hash and the gather in one launch, the row ids never
+    written.  Other arguments as ple_row_ids."""
+    where = "ple_row_embed"
+    if (req is None) != (local is None):
+        raise ValueError(f"{where}: pass both req and local, or neither (decode)")
+    dev = _one_cuda_device([t for t in (input_ids, req, local, ngram_context, layer_multipliers,
+                                        vocab_sizes, offsets, table, out) if t is not None], where)
+    if table.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{where}: table must be bfloat16 (or its 16-bit patterns)")
+    if table.dim() != 3 or not table.is_contiguous():
+        raise ValueError(f"{where}: table must be a contiguous [L, V, D] tensor")
+    M = layer_multipliers.reshape(1, -1) if layer_multipliers.dim() == 1 else layer_multipliers
+    vocab = vocab_sizes.reshape(1, -1) if vocab_sizes.dim() == 1 else vocab_sizes
+    off = offsets.reshape(1, -1) if offsets.dim() == 1 else offsets
+    for name, t in (("layer_multipliers", M), ("vocab_sizes", vocab), ("offsets", off)):
+        _need(t, torch.int64, name, where)
+    L, H = vocab.shape
+    T = input_ids.shape[0]
+    V, D = table.shape[1], table.shape[2]
+    if table.shape[0] != L or M.shape != (L, int(ngram_size)) or off.shape != (L, H):
+        raise ValueError(f"{where}: table [L, V, D], layer_multipliers [L, N], offsets [L, H]")
+    if input_ids.dtype not in (torch.int32, torch.int64) or ngram_context.dtype != input_ids.dtype:
+        raise TypeError(f"{where}: input_ids and ngram_context must share int32 or int64")
+    if req is not None:
+        for name, t in (("req", req), ("local", local)):
+            _need(t, torch.int32, name, where)
+    if out is None:
+        out = torch.empty((L, T, D), dtype=torch.float32, device=dev)
+    else:
+        _need(out, torch.float32, "out", where)
+        if tuple(out.shape) != (L, T, D):
+            raise ValueError(f"{where}: out must be [L, T, D]")
+    ctx = ngram_context
+    with torch.cuda.device(dev):
+        st = lib().ple_row_embed(
+            _ptr(input_ids), PLE_I64 if input_ids.dtype == torch.int64 else PLE_I32, T,
+            _ptr(req) if req is not None else ctypes.c_void_p(0),
+            _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx), ctx.shape[0],
+            ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, int(ngram_size),
+            int(heads_per_ngram), L, int(boundary_id), _ptr(table), V, D, _ptr(out),
+            _stream_handle(stream, dev))
     _check(st, where)
     return out
 

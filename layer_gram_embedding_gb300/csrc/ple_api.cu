@@ -76,13 +76,16 @@ extern "C" ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t n
 
 namespace {
 
-ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
-                        const int32_t* req, const int32_t* local, const void* ngram_context,
-                        int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
-                        const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
-                        int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
-                        int64_t boundary_id, void* out, int out_bytes, const int32_t* cu_seqlens,
-                        void* next_context, void* stream) {
+// Checks the arguments every row-id entry point shares and fills the kernel
+// parameters.  Returns PLE_OK with *empty set when there is nothing to do.
+ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                          const int32_t* req, const int32_t* local, const void* ngram_context,
+                          int32_t num_requests, int32_t ctx_len,
+                          const int64_t* layer_multipliers, const int64_t* vocab_sizes,
+                          const int64_t* offsets, int32_t num_heads, int32_t ngram_size,
+                          int32_t heads_per_ngram, int32_t num_layers, int64_t boundary_id,
+                          ple::RowIdsParams* p, bool* empty) {
+    *empty = false;
     // sizes first, then the page's two geometry preconditions
     if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
         num_tokens < 0 || num_tokens > INT32_MAX)
@@ -91,50 +94,77 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     if ((int64_t)num_heads != (int64_t)(ngram_size - 1) * heads_per_ngram)
         return PLE_ERR_GEOMETRY_HEADS;
     if (num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
-    if (out_bytes != 4 && out_bytes != 8) return PLE_ERR_DTYPE;
-    if (num_tokens == 0) return PLE_OK;
+    if (num_tokens == 0) {
+        *empty = true;
+        return PLE_OK;
+    }
     if (num_requests < 1) return PLE_ERR_SIZE;
     // both index pointers NULL: a decode batch, one token per request at offset 0
     const bool index_free = !req && !local;
     if (index_free && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
     if (!input_ids || (!index_free && (!req || !local)) || !ngram_context || !layer_multipliers ||
-        !vocab_sizes || !offsets || !out)
+        !vocab_sizes || !offsets)
         return PLE_ERR_NULL;
-    // the carry finds each request's last token (and empty requests) through
-    // cu_seqlens, except in an index-free decode
-    if (next_context && !index_free && !cu_seqlens) return PLE_ERR_NULL;
     if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
         !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
-        !aligned(offsets, 8) || !aligned(out, out_bytes) || !aligned(cu_seqlens, 4) ||
-        !aligned(next_context, id_bytes))
+        !aligned(offsets, 8))
+        return PLE_ERR_ALIGN;
+    p->ids = input_ids;
+    p->req = req;
+    p->local = local;
+    p->ctx = ngram_context;
+    p->mult = layer_multipliers;
+    p->vocab = vocab_sizes;
+    p->offsets = offsets;
+    p->out = nullptr;
+    p->T = num_tokens;
+    p->boundary = boundary_id;
+    p->B = num_requests;
+    p->N = ngram_size;
+    p->hpn = heads_per_ngram;
+    p->H = num_heads;
+    p->L = num_layers;
+    p->ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
+    p->out_vec_ok = 0;
+    p->index_free = index_free ? 1 : 0;
+    p->out_bytes = 8;
+    p->cu = nullptr;
+    p->next_ctx = nullptr;
+    return PLE_OK;
+}
+
+ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                        const int32_t* req, const int32_t* local, const void* ngram_context,
+                        int32_t num_requests, int32_t ctx_len, const int64_t* layer_multipliers,
+                        const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
+                        int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
+                        int64_t boundary_id, void* out, int out_bytes, const int32_t* cu_seqlens,
+                        void* next_context, void* stream) {
+    ple::RowIdsParams p;
+    bool empty = false;
+    ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
+                                   num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
+                                   num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
+                                   &p, &empty);
+    if (st != PLE_OK) return st;
+    if (out_bytes != 4 && out_bytes != 8) return PLE_ERR_DTYPE;
+    if (empty) return PLE_OK;
+    if (!out) return PLE_ERR_NULL;
+    // the carry finds each request's last token (and empty requests) through
+    // cu_seqlens, except in an index-free decode
+    if (next_context && !p.index_free && !cu_seqlens) return PLE_ERR_NULL;
+    const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
+    if (!aligned(out, out_bytes) || !aligned(cu_seqlens, 4) || !aligned(next_context, id_bytes))
         return PLE_ERR_ALIGN;
 
     (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
-
-    ple::RowIdsParams p;
-    p.ids = input_ids;
-    p.req = req;
-    p.local = local;
-    p.ctx = ngram_context;
-    p.mult = layer_multipliers;
-    p.vocab = vocab_sizes;
-    p.offsets = offsets;
     p.out = out;
-    p.T = num_tokens;
-    p.boundary = boundary_id;
-    p.B = num_requests;
-    p.N = ngram_size;
-    p.hpn = heads_per_ngram;
-    p.H = num_heads;
-    p.L = num_layers;
-    p.ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
     p.out_vec_ok = aligned(out, 16) ? 1 : 0;
-    p.index_free = index_free ? 1 : 0;
     p.out_bytes = out_bytes;
     p.cu = next_context ? cu_seqlens : nullptr;
     p.next_ctx = next_context;
@@ -190,6 +220,46 @@ extern "C" ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, in
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
                         heads_per_ngram, num_layers, boundary_id, out, out_bytes, cu_seqlens,
                         next_context, stream);
+}
+
+extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
+                                    const int32_t* req, const int32_t* local,
+                                    const void* ngram_context, int32_t num_requests,
+                                    int32_t ctx_len, const int64_t* layer_multipliers,
+                                    const int64_t* vocab_sizes, const int64_t* offsets,
+                                    int32_t num_heads, int32_t ngram_size,
+                                    int32_t heads_per_ngram, int32_t num_layers,
+                                    int64_t boundary_id, const void* table, int64_t table_rows,
+                                    int32_t dim, float* out, void* stream) {
+    ple::RowIdsParams p;
+    bool empty = false;
+    ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
+                                   num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
+                                   num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
+                                   &p, &empty);
+    if (st != PLE_OK) return st;
+    if (dim < 8 || dim % 8 != 0 || dim > PLE_MAX_EMBED_DIM || table_rows < 0) return PLE_ERR_SIZE;
+    // the table's byte size must fit in 64 bits
+    if (table_rows > INT64_MAX / ((int64_t)num_layers * dim * 2)) return PLE_ERR_SIZE;
+    if (empty) return PLE_OK;
+    if (!out || (table_rows > 0 && !table)) return PLE_ERR_NULL;
+    if (!aligned(table, 16) || !aligned(out, 16)) return PLE_ERR_ALIGN;
+
+    (void)cudaGetLastError();
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+    ple::EmbedArgs ea;
+    ea.table = static_cast<const uint16_t*>(table);
+    ea.rows = table_rows;
+    ea.dim = dim;
+    ea.out = out;
+    const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev, /*runtime_layout=*/true);
+    if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
+    e = ple::launch_row_embed(p, ea, id_dtype == PLE_I32 ? 4 : 8, cfg,
+                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
 }
 
 extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,

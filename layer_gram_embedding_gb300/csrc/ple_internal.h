@@ -50,6 +50,15 @@ struct RowIdsParams {
     void* next_ctx;         // [B, N-1] carried context out, dtype of ids (NULL: none)
 };
 
+// The table gather fused with the hash: table [L, rows, dim] bfloat16 bits,
+// out [L, T, dim] float.
+struct EmbedArgs {
+    const uint16_t* table;
+    int64_t rows;
+    int32_t dim;
+    float* out;
+};
+
 struct RowIdsLaunch {
     dim3 grid;
     dim3 block;
@@ -65,13 +74,18 @@ struct DeviceFacts {
 cudaError_t device_facts(DeviceFacts* out);
 
 // Chooses grid/block/shared memory and fills p.group_layers / p.stage_pitch.
-RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev);
+// runtime_layout: size the shared memory for the runtime-shape kernel's
+// staging whatever the shape (the fused table gather uses that layout).
+RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_layout = false);
 cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                            cudaStream_t stream);
 // The tuned (ngram_size, heads_per_ngram) pairs of the fixed-shape kernel.
 bool shape_is_fixed(int N, int hpn);
 cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                  cudaStream_t stream);
+
+cudaError_t launch_row_embed(const RowIdsParams& p, const EmbedArgs& e, int id_bytes,
+                             const RowIdsLaunch& cfg, cudaStream_t stream);
 
 cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                int32_t* req, int32_t* local, const DeviceFacts& dev,

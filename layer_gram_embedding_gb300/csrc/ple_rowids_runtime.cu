@@ -102,11 +102,11 @@ static bool uses_fixed_kernel(const RowIdsParams& p) {
     return !p.index_free && shape_is_fixed(p.N, p.hpn);
 }
 
-RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev) {
+RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_layout) {
     RowIdsLaunch cfg;
     const int64_t tiles = (p.T + kTileTokens - 1) / kTileTokens;
     int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
-    const bool fixed_shape = uses_fixed_kernel(p);
+    const bool fixed_shape = !runtime_layout && uses_fixed_kernel(p);
     p.stage_pitch = p.H | 1;
     const size_t per_warp =
         (size_t)(kHaloSlots + kTileTokens) * 8 + stage_bytes(p.H, fixed_shape);

@@ -246,6 +246,62 @@ def test_chunked_prefill_through_the_carry_equals_one_prefill():
     assert_same(got, whole, "chunked prefill through the carry")
 
 
+def check_embed(batch, table, index_free=False, what=""):
+    """GPU gather vs the oracle's exact (double) sum: fp32 recursive summation
+    of H terms errs by at most (H-1) * 2^-24 * sum|x| per element."""
+    t = torch.from_numpy(table.view(np.int16)).to(DEV)
+    if index_free:
+        req = local = None
+    else:
+        req, local = gpu_index(batch)
+    got = ple.ple_row_embed(dev(batch.ids), req, local, dev(batch.ngram_context),
+                            dev(batch.layer_multipliers), dev(batch.vocab_sizes),
+                            dev(batch.offsets), batch.ngram_size, batch.heads_per_ngram,
+                            batch.boundary_id, t).cpu().numpy().astype(np.float64)
+    oreq, olocal = oracle_index(batch)
+    exact, abs_sum = oracle.row_embed(batch.ids, oreq, olocal, batch.ngram_context,
+                                      batch.layer_multipliers, batch.vocab_sizes, batch.offsets,
+                                      batch.ngram_size, batch.heads_per_ngram, batch.boundary_id,
+                                      table)
+    bound = (batch.num_heads - 1) * 2.0 ** -24 * abs_sum
+    err = np.abs(got - exact)
+    assert got.shape == exact.shape
+    assert np.all(err <= bound), (what, float(err.max()), float((err - bound).max()))
+
+
+@pytest.mark.parametrize("D", [8, 16, 24, 64, 256, 264])
+def test_row_embed_random_batches(D):
+    for seed in range(12):
+        batch, table = wl.small_table_batch(12000 + 31 * D + seed, D=D, T_max=150,
+                                            ids_dtype=np.int32 if seed % 2 else np.int64)
+        check_embed(batch, table, what=f"D={D} seed={seed}")
+
+
+def test_row_embed_rows_outside_the_table_add_nothing():
+    batch, table = wl.small_table_batch(777, D=32, T_max=200, L=2)
+    check_embed(batch, np.ascontiguousarray(table[:, : table.shape[1] // 3]), what="short table")
+
+
+def test_row_embed_decode_without_an_index():
+    b = wl.decode(8)
+    rng = np.random.default_rng(8)
+    vocab = wl.random_primes(rng, 4, 2, 3000).reshape(1, 4)
+    b = dataclasses.replace(b, vocab_sizes=vocab, offsets=wl.prefix_offsets(vocab))
+    table = wl.embed_table(rng, 1, int(vocab.sum()), 128)
+    check_embed(b, table, index_free=True, what="decode")
+    check_embed(b, table, index_free=False, what="decode with index")
+
+
+def test_row_embed_large_prefill_sample():
+    """The large-prefill shape (N=4, 12 heads, 8 layers, int64 ids) on the
+    first 20000 tokens, D=64, with a table cut to 2^16 rows per layer so that
+    most row ids fall outside it (the out-of-range rule at scale)."""
+    full = wl.prefill_262144()
+    batch = wl.slice_batch(full, 0, 20000)
+    rng = np.random.default_rng(3)
+    check_embed(batch, wl.embed_table(rng, 8, 2 ** 16, 64), what="prefill sample")
+
+
 @pytest.mark.parametrize("chunk", range(6))
 def test_random_edge_batches(chunk):
     """Small ragged batches spanning several 64-token tiles with ragged tails,

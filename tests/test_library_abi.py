@@ -125,6 +125,32 @@ def test_row_ids_ex_host_checks(lib, kw, status):
     assert row_ids_ex(lib, **kw) == status
 
 
+def row_embed(lib, **kw):
+    a = dict(ids=A, dtype=1, T=64, req=A, local=A, ctx=A, B=1, ctx_len=2, M=A, vocab=A, off=A,
+             H=4, N=3, hpn=2, L=1, b=7, table=A, V=100, D=64, out=A)
+    a.update(kw)
+    return lib.ple_row_embed(a["ids"], a["dtype"], a["T"], a["req"], a["local"], a["ctx"],
+                             a["B"], a["ctx_len"], a["M"], a["vocab"], a["off"], a["H"], a["N"],
+                             a["hpn"], a["L"], a["b"], a["table"], a["V"], a["D"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ctx_len=1), ple.PLE_ERR_GEOMETRY_CTX),
+    (dict(D=4), ple.PLE_ERR_SIZE),
+    (dict(D=12), ple.PLE_ERR_SIZE),
+    (dict(D=65544), ple.PLE_ERR_SIZE),
+    (dict(V=-1), ple.PLE_ERR_SIZE),
+    (dict(V=2 ** 62), ple.PLE_ERR_SIZE),
+    (dict(table=None), ple.PLE_ERR_NULL),
+    (dict(out=None), ple.PLE_ERR_NULL),
+    (dict(table=A + 8), ple.PLE_ERR_ALIGN),
+    (dict(out=A + 4), ple.PLE_ERR_ALIGN),
+    (dict(T=0, table=None, out=None), ple.PLE_OK),
+])
+def test_row_embed_host_checks(lib, kw, status):
+    assert row_embed(lib, **kw) == status
+
+
 def test_row_ids_empty_batch_is_ok_without_pointers(lib):
     assert row_ids(lib, T=0, ids=None, req=None, local=None, ctx=None, M=None, vocab=None,
                    off=None, out=None, B=0) == ple.PLE_OK
