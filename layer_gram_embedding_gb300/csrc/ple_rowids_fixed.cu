@@ -184,9 +184,11 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                 const int h = (s - 1) * HPT + j;
                 const uint4 c0 = hf[h];
                 const uint4 c1 = hf[h + 1];
-                stAw[lane * P2 + h / 2] = make_uint2(floormod_fast(uA, c0), floormod_fast(uA, c1));
+                const uint32_t n0 = c0.z << 1, n1 = c1.z << 1;  // -2v of each head
+                stAw[lane * P2 + h / 2] =
+                    make_uint2(floormod_fast(uA, c0, n0), floormod_fast(uA, c1, n1));
                 stAw[(32 + lane) * P2 + h / 2] =
-                    make_uint2(floormod_fast(uB, c0), floormod_fast(uB, c1));
+                    make_uint2(floormod_fast(uB, c0, n0), floormod_fast(uB, c1, n1));
             }
         }
         __syncwarp();
