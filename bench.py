@@ -631,6 +631,11 @@ def embed_bench(args):
     lib_build.build()
     device = torch.device("cuda", 0)
     b = wl.prefill_262144()
+    if args.embed_layers < b.num_layers:
+        # fewer layers keep a profiling capture within a few GB of table
+        k = max(1, args.embed_layers)
+        b = wl.replace(b, layer_multipliers=b.layer_multipliers[:k], vocab_sizes=b.vocab_sizes[:k],
+                       offsets=b.offsets[:k])
     T, B, L, H, N = b.num_tokens, b.num_requests, b.num_layers, b.num_heads, b.ngram_size
     D = args.embed_dim
     V = int(b.vocab_sizes.sum(axis=1).max())
@@ -691,6 +696,8 @@ def main(argv=None):
     ap.add_argument("--embed", action="store_true",
                     help="time the fused table gather instead of the contract line")
     ap.add_argument("--embed-dim", type=int, default=256)
+    ap.add_argument("--embed-layers", type=int, default=8,
+                    help="layers of the large prefill the gather runs (default all 8)")
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload (graph of 300 calls) instead of the contract line")
     args = ap.parse_args(argv)

@@ -2,7 +2,9 @@
 //
 // Compiled for the PLE configurations this library is tuned for -- (ngram
 // size, heads per order) in {(3,2), (3,4), (4,4), (5,8)}, each with int32 or
-// int64 ids, int64 or int32 row ids, with or without the context carry.
+// int64 ids, int64 or int32 row ids, with or without the context carry, with
+// or without an index (the index-free decode) -- every choice at compile
+// time, because a run-time branch in the window costs the large prefill.
 // Each lane hashes two tokens of the 64-token tile (lane and lane + 32) per
 // shared constant load; the fast path stages 32-bit remainders as head pairs
 // in rows of odd pitch (8-byte stores hit 16 distinct bank pairs per half
@@ -75,7 +77,7 @@ __device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int*
     }
 }
 
-template <typename IdT, int NT, int HPT, typename OutT, bool kCarry>
+template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, bool kIndexFree>
 __global__ void __launch_bounds__(kMaxWarps * 32)
 row_ids_fixed_kernel(const RowIdsParams p) {
     static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
@@ -108,8 +110,8 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     if (ntile > 0) {
         stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
         int32_t rA, qA, rB, qB;
-        window<IdT, N, N, false>(p, ids_s, t0, lane, lane < nA, N, VA, rA, qA);
-        window<IdT, N, N, false>(p, ids_s, t0, 32 + lane, lane < nB, N, VB, rB, qB);
+        window<IdT, N, N, kIndexFree>(p, ids_s, t0, lane, lane < nA, N, VA, rA, qA);
+        window<IdT, N, N, kIndexFree>(p, ids_s, t0, 32 + lane, lane < nB, N, VB, rB, qB);
         if (kCarry && blockIdx.y == 0) {
             carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
             carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
@@ -248,17 +250,21 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     }
 }
 
-template <typename IdT, typename OutT, bool kCarry>
+template <typename IdT, typename OutT, bool kCarry, bool kIndexFree>
 KernelFn pick_fixed(int N, int hpn) {
-    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT, kCarry>;
-    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT, kCarry>;
-    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT, kCarry>;
-    return row_ids_fixed_kernel<IdT, 5, 8, OutT, kCarry>;
+    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT, kCarry, kIndexFree>;
+    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT, kCarry, kIndexFree>;
+    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT, kCarry, kIndexFree>;
+    return row_ids_fixed_kernel<IdT, 5, 8, OutT, kCarry, kIndexFree>;
 }
 
 template <typename IdT, typename OutT>
-KernelFn pick_fixed(int N, int hpn, bool carry) {
-    return carry ? pick_fixed<IdT, OutT, true>(N, hpn) : pick_fixed<IdT, OutT, false>(N, hpn);
+KernelFn pick_fixed(int N, int hpn, bool carry, bool index_free) {
+    if (index_free)
+        return carry ? pick_fixed<IdT, OutT, true, true>(N, hpn)
+                     : pick_fixed<IdT, OutT, false, true>(N, hpn);
+    return carry ? pick_fixed<IdT, OutT, true, false>(N, hpn)
+                 : pick_fixed<IdT, OutT, false, false>(N, hpn);
 }
 
 }  // namespace
@@ -266,13 +272,14 @@ KernelFn pick_fixed(int N, int hpn, bool carry) {
 cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                  cudaStream_t stream) {
     const bool carry = p.next_ctx != nullptr;
+    const bool free = p.index_free != 0;
     KernelFn fn;
     if (p.out_bytes == 4)
-        fn = id_bytes == 4 ? pick_fixed<int32_t, int32_t>(p.N, p.hpn, carry)
-                           : pick_fixed<int64_t, int32_t>(p.N, p.hpn, carry);
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int32_t>(p.N, p.hpn, carry, free)
+                           : pick_fixed<int64_t, int32_t>(p.N, p.hpn, carry, free);
     else
-        fn = id_bytes == 4 ? pick_fixed<int32_t, int64_t>(p.N, p.hpn, carry)
-                           : pick_fixed<int64_t, int64_t>(p.N, p.hpn, carry);
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int64_t>(p.N, p.hpn, carry, free)
+                           : pick_fixed<int64_t, int64_t>(p.N, p.hpn, carry, free);
     return launch_fn(fn, p, cfg, stream);
 }
 

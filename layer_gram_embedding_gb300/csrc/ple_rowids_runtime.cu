@@ -95,12 +95,9 @@ bool shape_is_fixed(int N, int hpn) {
     return (N == 3 && (hpn == 2 || hpn == 4)) || (N == 4 && hpn == 4) || (N == 5 && hpn == 8);
 }
 
-// The fixed-shape kernel takes the tuned shapes; the index-free decode runs
-// the runtime-shape kernel (a decode is launch-bound, and keeping the
-// index-free branch out of the fixed kernel keeps its large-prefill speed).
-static bool uses_fixed_kernel(const RowIdsParams& p) {
-    return !p.index_free && shape_is_fixed(p.N, p.hpn);
-}
+// The fixed-shape kernel takes the tuned shapes, the runtime-shape kernel
+// every other one.
+static bool uses_fixed_kernel(const RowIdsParams& p) { return shape_is_fixed(p.N, p.hpn); }
 
 RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_layout) {
     RowIdsLaunch cfg;
