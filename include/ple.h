@@ -231,6 +231,31 @@ ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_to
                          float* out, void* stream);
 
 /*
+ * ple_validate_index -- diagnostic: check the index preconditions on the
+ * device.
+ *
+ * ple_row_ids documents device-data preconditions on req / local that the
+ * host cannot check without reading device memory; the kernel clamps such
+ * data into range but the rows are then unspecified.  This call checks them
+ * against their definition (section "What", second observation; "Why it is
+ * safe", the decode rule): req[t] = r with cu_seqlens[r] <= t <
+ * cu_seqlens[r+1] and local[t] = t - cu_seqlens[r], or req[t] = t and
+ * local[t] = 0 for a decode.
+ *
+ *   cu_seqlens, num_requests, num_tokens, is_decode: as ple_build_token_index.
+ *   req, local   [T] int32, device: the index to check.
+ *   first_bad    one int64, device, 8-byte aligned.  The caller stores a
+ *                value >= T there before the call; the call lowers it to the
+ *                first token whose (req, local) is wrong and leaves it alone
+ *                when every token is right.  Read it after the stream runs.
+ *
+ * Errors: PLE_ERR_NULL, PLE_ERR_SIZE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ */
+ple_status ple_validate_index(const int32_t* cu_seqlens, int32_t num_requests,
+                              int64_t num_tokens, int32_t is_decode, const int32_t* req,
+                              const int32_t* local, int64_t* first_bad, void* stream);
+
+/*
  * ple_selftest_floor_mod -- diagnostic: the library's invariant-divisor
  * floored remainder next to one computed with CUDA's own % operator.
  *

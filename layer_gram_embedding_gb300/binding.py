@@ -48,6 +48,7 @@ SIGNATURES = {
                               _I32, _I32, _I64, _P, _I32, _P, _P, _P]),
     "ple_row_embed": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
                              _I32, _I32, _I64, _P, _I64, _I32, _P, _P]),
+    "ple_validate_index": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P, _P]),
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
@@ -301,6 +302,29 @@ def ple_row_embed(input_ids: torch.Tensor, req: torch.Tensor | None, local: torc
             _stream_handle(stream, dev))
     _check(st, where)
     return out
+
+
+def ple_validate_index(cu_seqlens, num_requests: int, num_tokens: int, is_decode: bool,
+                       req: torch.Tensor, local: torch.Tensor, stream=None) -> torch.Tensor:
+    """A one-element int64 CUDA tensor: the first token whose (req, local)
+    is not what cu_seqlens (or the decode rule) defines, or num_tokens when
+    every token is right.  Asynchronous: read it when the stream has run."""
+    where = "ple_validate_index"
+    dev = _one_cuda_device([t for t in (cu_seqlens if not is_decode else None, req, local)
+                            if t is not None], where)
+    for name, t in (("req", req), ("local", local)):
+        _need(t, torch.int32, name, where)
+    first_bad = torch.full((1,), int(num_tokens), dtype=torch.int64, device=dev)
+    cu_p = ctypes.c_void_p(0)
+    if not is_decode:
+        _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+        cu_p = _ptr(cu_seqlens)
+    with torch.cuda.device(dev):
+        st = lib().ple_validate_index(cu_p, int(num_requests), int(num_tokens),
+                                      int(bool(is_decode)), _ptr(req), _ptr(local),
+                                      _ptr(first_bad), _stream_handle(stream, dev))
+    _check(st, where)
+    return first_bad
 
 
 def ple_selftest_floor_mod(x: torch.Tensor, v: torch.Tensor, stream=None):

@@ -262,6 +262,28 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     return PLE_OK;
 }
 
+extern "C" ple_status ple_validate_index(const int32_t* cu_seqlens, int32_t num_requests,
+                                         int64_t num_tokens, int32_t is_decode,
+                                         const int32_t* req, const int32_t* local,
+                                         int64_t* first_bad, void* stream) {
+    if (num_tokens < 0 || num_tokens > INT32_MAX) return PLE_ERR_SIZE;
+    if (num_tokens == 0) return PLE_OK;
+    if (num_requests < 1) return PLE_ERR_SIZE;
+    if (is_decode && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
+    if (!req || !local || !first_bad || (!is_decode && !cu_seqlens)) return PLE_ERR_NULL;
+    if (!aligned(req, 4) || !aligned(local, 4) || !aligned(first_bad, 8) ||
+        (!is_decode && !aligned(cu_seqlens, 4)))
+        return PLE_ERR_ALIGN;
+    (void)cudaGetLastError();
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+    e = ple::launch_validate_index(cu_seqlens, num_requests, num_tokens, is_decode, req, local,
+                                   first_bad, dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
+}
+
 extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
                                              int64_t* out_fast, int64_t* out_ref, void* stream) {
     if (n < 0) return PLE_ERR_SIZE;

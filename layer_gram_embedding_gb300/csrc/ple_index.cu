@@ -95,6 +95,39 @@ token_index_prefill_kernel(const int32_t* __restrict__ cu, int32_t B, int64_t T,
     }
 }
 
+// First token whose (req, local) differs from the index cu_seqlens (or the
+// decode rule) defines; *first_bad is lowered to it with an atomic min.
+__global__ void __launch_bounds__(kIndexThreads)
+validate_index_kernel(const int32_t* __restrict__ cu, int32_t B, int64_t T, int32_t is_decode,
+                      const int32_t* __restrict__ req, const int32_t* __restrict__ local,
+                      unsigned long long* __restrict__ first_bad) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t bad = INT64_MAX;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += stride) {
+        int32_t r_exp, l_exp;
+        if (is_decode) {
+            r_exp = (int32_t)t;
+            l_exp = 0;
+        } else {
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                const int mid = lo + ((hi - lo + 1) >> 1);
+                if ((int64_t)__ldg(cu + mid) <= t)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            r_exp = lo;
+            l_exp = (int32_t)(t - (int64_t)__ldg(cu + lo));
+        }
+        if (__ldg(req + t) != r_exp || __ldg(local + t) != l_exp) {
+            bad = t;
+            break;  // later tokens of this thread are larger
+        }
+    }
+    if (bad != INT64_MAX) atomicMin(first_bad, (unsigned long long)bad);
+}
+
 __global__ void __launch_bounds__(kIndexThreads)
 selftest_floor_mod_kernel(const int64_t* __restrict__ x, const int64_t* __restrict__ v, int64_t n,
                           int64_t* __restrict__ out_fast, int64_t* __restrict__ out_ref) {
@@ -160,6 +193,14 @@ cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t 
                    : launch_pdl(token_index_prefill_kernel<false, false>, g, stream, cu, B, T, req, local);
     }
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
+                                  const int32_t* req, const int32_t* local, int64_t* first_bad,
+                                  const DeviceFacts& dev, cudaStream_t stream) {
+    validate_index_kernel<<<grid_for(T, dev), kIndexThreads, 0, stream>>>(
+        cu, B, T, is_decode, req, local, reinterpret_cast<unsigned long long*>(first_bad));
     return cudaGetLastError();
 }
 

@@ -91,6 +91,10 @@ cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t 
                                int32_t* req, int32_t* local, const DeviceFacts& dev,
                                cudaStream_t stream);
 
+cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
+                                  const int32_t* req, const int32_t* local, int64_t* first_bad,
+                                  const DeviceFacts& dev, cudaStream_t stream);
+
 cudaError_t launch_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
                                       int64_t* out_fast, int64_t* out_ref, const DeviceFacts& dev,
                                       cudaStream_t stream);

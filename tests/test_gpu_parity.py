@@ -100,6 +100,34 @@ def test_token_index_paths(decode):
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
+def test_validate_index_accepts_the_built_index(name):
+    batch = WORKLOADS[name]
+    req, local = gpu_index(batch)
+    cu = dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None
+    first = ple.ple_validate_index(cu, batch.num_requests, batch.num_tokens, batch.is_decode,
+                                   req, local)
+    assert int(first) == batch.num_tokens
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_validate_index_finds_the_first_wrong_token(decode):
+    batch = wl.mixed_8192() if not decode else wl.random_batch(5, decode_batch=True, T_max=5000)
+    cu = dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None
+    rng = np.random.default_rng(17)
+    for trial in range(6):
+        req, local = gpu_index(batch)
+        T = batch.num_tokens
+        picks = rng.choice(T, size=int(rng.integers(1, 5)), replace=False)
+        for t in picks:
+            if rng.random() < 0.5:
+                req[int(t)] += 1
+            else:
+                local[int(t)] -= 1
+        first = ple.ple_validate_index(cu, batch.num_requests, T, batch.is_decode, req, local)
+        assert int(first) == int(picks.min())
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
 def test_row_ids_match_oracle_full_size(name):
     """Every workload at its full size, in the launch configuration the
     benchmark uses, compared element by element."""

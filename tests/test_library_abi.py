@@ -212,3 +212,17 @@ def test_library_has_no_host_compute_path():
 def test_bench_kernel_source_list_exists():
     import bench
     assert len(bench.kernel_source_hash()) == 16
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, 2, -1, 0, A, A, A), ple.PLE_ERR_SIZE),
+    ((A, 0, 5, 0, A, A, A), ple.PLE_ERR_SIZE),
+    ((None, 3, 5, 1, A, A, A), ple.PLE_ERR_SIZE),
+    ((None, 2, 5, 0, A, A, A), ple.PLE_ERR_NULL),
+    ((A, 2, 5, 0, A, A, None), ple.PLE_ERR_NULL),
+    ((A, 2, 5, 0, A, A, A + 4), ple.PLE_ERR_ALIGN),
+    ((A, 2, 5, 0, A + 2, A, A), ple.PLE_ERR_ALIGN),
+    ((None, 0, 0, 0, None, None, None), ple.PLE_OK),
+])
+def test_validate_index_host_checks(lib, args, status):
+    assert lib.ple_validate_index(*args, None) == status
