@@ -16,6 +16,12 @@ constexpr int kHaloSlots = 16;
 #define PLE_MAX_WARPS 4
 #endif
 constexpr int kMaxWarps = PLE_MAX_WARPS;
+// Register cap for the fixed-shape kernel: the minimum resident blocks per SM
+// passed to __launch_bounds__ (0 leaves the choice to the compiler).
+#ifndef PLE_FIXED_MIN_BLOCKS
+#define PLE_FIXED_MIN_BLOCKS 0
+#endif
+constexpr int kFixedMinBlocks = PLE_FIXED_MIN_BLOCKS;
 // Launch-shape target: thread blocks per SM the layer grouping aims for.
 #ifndef PLE_BLOCKS_PER_SM
 #define PLE_BLOCKS_PER_SM 16

@@ -85,7 +85,9 @@ __device__ __forceinline__ void load_tile_vec<int32_t>(const int32_t* src, int64
 
 // Per-block shared-memory layout, in order (all offsets 16-byte aligned):
 //   head constants of the layer group, structure of arrays:
-//     fast [G*H] uint4, off [G*H] int64 (padded to even), ext [G*H] uint4
+//     fast [G*H] uint4, off [G*H] int64 (padded to even), ext [G*H] uint4,
+//     off32 [G*H] the offsets' low words (padded to a multiple of 4), read
+//     four at a time by the int32 readout
 //   multipliers [G*N] int64 (padded to even)
 //   per warp: ids [kHaloSlots + kTileTokens] int64
 //   per warp: staging, stage_bytes(...) bytes
@@ -93,13 +95,15 @@ struct SmemLayout {
     uint4* fast;
     int64_t* off;
     uint4* ext;
+    int32_t* off32;
     int64_t* mul;
     int64_t* ids;
     unsigned char* stage;
 };
 
 __host__ __device__ constexpr size_t head_const_bytes(int heads) {
-    return (size_t)heads * 16 + (size_t)((heads + 1) & ~1) * 8 + (size_t)heads * 16;
+    return (size_t)heads * 16 + (size_t)((heads + 1) & ~1) * 8 + (size_t)heads * 16 +
+           (size_t)((heads + 3) & ~3) * 4;
 }
 
 // Staging bytes per warp.  Fixed shapes (even heads_per_ngram): 64 rows of
@@ -120,6 +124,7 @@ __device__ __forceinline__ SmemLayout carve_smem(unsigned char* base, int G, int
     s.fast = reinterpret_cast<uint4*>(base);
     s.off = reinterpret_cast<int64_t*>(base + (size_t)gh * 16);
     s.ext = reinterpret_cast<uint4*>(base + (size_t)gh * 16 + (size_t)((gh + 1) & ~1) * 8);
+    s.off32 = reinterpret_cast<int32_t*>(base + (size_t)gh * 32 + (size_t)((gh + 1) & ~1) * 8);
     s.mul = reinterpret_cast<int64_t*>(base + head_const_bytes(gh));
     s.ids = s.mul + ((G * N + 1) & ~1);
     s.stage = reinterpret_cast<unsigned char*>(s.ids + nwarps * (kHaloSlots + kTileTokens));
@@ -139,6 +144,7 @@ __device__ __forceinline__ int load_group_constants(const RowIdsParams& p, const
         sm.fast[i] = c.fast;
         sm.off[i] = c.off;
         sm.ext[i] = c.ext;
+        sm.off32[i] = (int32_t)c.off;
         fast &= (c.ext.z == kHeadFast) ? 1 : 0;
     }
     for (int i = threadIdx.x; i < gl * N; i += blockDim.x) sm.mul[i] = p.mult[(int64_t)l0 * N + i];
@@ -166,15 +172,14 @@ __device__ __forceinline__ void stage_ids(const RowIdsParams& p, int64_t* ids_s,
 }
 
 // The shifted window V(t, 0..N-1) of tile token i with the carried boundary
-// predicate.  Index data outside the addressable ranges is clamped; the
-// clamped request and offset are returned for the context carry.  The
-// index-free decode is a compile-time choice: a run-time branch here costs
-// the large-prefill kernel about 3% (measured on GB300).
-template <typename IdT, int NMAX, int NT, bool kIndexFree>
-__device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids_s, int64_t t0,
-                                       int i, bool live, int N, int64_t (&V)[NMAX],
-                                       int32_t& r_out, int32_t& q_out) {
-    const int64_t t = t0 + i;
+// predicate, in two steps so a kernel can issue the index loads early:
+// load_index reads (req, local) and clamps index data outside the
+// addressable ranges; window_at builds V.  The index-free decode is a
+// compile-time choice: a run-time branch here costs the large-prefill
+// kernel about 3% (measured on GB300).
+template <bool kIndexFree>
+__device__ __forceinline__ void load_index(const RowIdsParams& p, int64_t t, bool live,
+                                           int32_t& r_out, int32_t& q_out) {
     int32_t r = 0, q = 0;
     if (kIndexFree) {
         // a decode batch without an index: every token is its own request
@@ -183,10 +188,15 @@ __device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids
         r = __ldg(p.req + t);
         q = __ldg(p.local + t);
     }
-    r = min(max(r, 0), p.B - 1);
-    q = (int32_t)min((int64_t)max(q, 0), t);
-    r_out = r;
-    q_out = q;
+    r_out = min(max(r, 0), p.B - 1);
+    q_out = (int32_t)min((int64_t)max(q, 0), t);
+}
+
+// The window of tile token i from its (clamped) request r and offset q.
+template <typename IdT, int NMAX, int NT>
+__device__ __forceinline__ void window_at(const RowIdsParams& p, const int64_t* ids_s, int i,
+                                          bool live, int N, int32_t r, int32_t q,
+                                          int64_t (&V)[NMAX]) {
     V[0] = live ? ids_s[i] : 0;
     const IdT* crow = static_cast<const IdT*>(p.ctx) + (int64_t)r * (N - 1) + (N - 1) + q;
     bool valid = true;
@@ -197,6 +207,14 @@ __device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids
         valid = valid && (w != p.boundary);
         V[s] = valid ? w : p.boundary;
     }
+}
+
+template <typename IdT, int NMAX, int NT, bool kIndexFree>
+__device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids_s, int64_t t0,
+                                       int i, bool live, int N, int64_t (&V)[NMAX],
+                                       int32_t& r_out, int32_t& q_out) {
+    load_index<kIndexFree>(p, t0 + i, live, r_out, q_out);
+    window_at<IdT, NMAX, NT>(p, ids_s, i, live, N, r_out, q_out, V);
 }
 
 // The context carry: the last token of each request writes the request's

@@ -78,7 +78,7 @@ __device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int*
 }
 
 template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, bool kIndexFree>
-__global__ void __launch_bounds__(kMaxWarps * 32)
+__global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_fixed_kernel(const RowIdsParams p) {
     static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
     constexpr int N = NT;
@@ -108,10 +108,14 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
     int64_t VA[N], VB[N];
     if (ntile > 0) {
-        stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+        // the index loads go out before the ids staging so the two round
+        // trips overlap
         int32_t rA, qA, rB, qB;
-        window<IdT, N, N, kIndexFree>(p, ids_s, t0, lane, lane < nA, N, VA, rA, qA);
-        window<IdT, N, N, kIndexFree>(p, ids_s, t0, 32 + lane, lane < nB, N, VB, rB, qB);
+        load_index<kIndexFree>(p, t0 + lane, lane < nA, rA, qA);
+        load_index<kIndexFree>(p, t0 + 32 + lane, lane < nB, rB, qB);
+        stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+        window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
+        window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
         if (kCarry && blockIdx.y == 0) {
             carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
             carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
@@ -226,8 +230,7 @@ row_ids_fixed_kernel(const RowIdsParams p) {
             for (int k = 0; k < NU; ++k) {
                 int col = r0 + k * GU;
                 col = col >= KU ? col - KU : col;
-                const int64_t* o = sm.off + l * H + 4 * col;
-                offs[k] = make_int4((int)o[0], (int)o[1], (int)o[2], (int)o[3]);
+                offs[k] = *reinterpret_cast<const int4*>(sm.off32 + l * H + 4 * col);
             }
             int* d = reinterpret_cast<int*>(dst);
             if (full && vec_out) {
