@@ -140,6 +140,9 @@ ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests
  * local NULL, or any other pointer), PLE_ERR_SIZE (both NULL with B != T),
  * PLE_ERR_DTYPE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
  * One kernel launch; no host reads; fixed grid for fixed (T, L, H, N).
+ * Batches of at most ple_small_batch_max_rows() row ids (T * H * L) run the
+ * small-batch kernel, one thread per row id; larger ones the tiled kernels.
+ * The row ids are the same either way.
  */
 ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
                        const int32_t* req, const int32_t* local, const void* ngram_context,
@@ -274,6 +277,13 @@ ple_status ple_validate_index(const int32_t* cu_seqlens, int32_t num_requests,
  */
 ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
                                   int64_t* out_fast, int64_t* out_ref, void* stream);
+
+/* The largest batch, in row ids (T * H * L, with L <= 65535), that the
+ * row-id entry points hash with the small-batch kernel: latency-bound
+ * decode steps and short prefills, one thread per row id, no block barrier.
+ * A library tuning constant with no counterpart on the page; the row ids do
+ * not depend on it. */
+int64_t ple_small_batch_max_rows(void);
 
 /* Static, NUL-terminated description of a status code ("unknown status"
  * for values outside ple_status). */

@@ -52,6 +52,7 @@ SIGNATURES = {
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
+    "ple_small_batch_max_rows": (_I64, []),
 }
 
 _lock = threading.Lock()
@@ -90,6 +91,12 @@ def lib() -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return lib().ple_status_string(int(status)).decode()
+
+
+def small_batch_max_rows() -> int:
+    """Batches of at most this many row ids (T * H * L) run the small-batch
+    kernel; the row ids do not depend on which kernel runs."""
+    return int(lib().ple_small_batch_max_rows())
 
 
 def _check(status: int, where: str):

@@ -317,3 +317,5 @@ extern "C" const char* ple_status_string(int32_t status) {
 }
 
 extern "C" int32_t ple_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int64_t ple_small_batch_max_rows(void) { return ple::kSmallMaxRows; }

@@ -29,6 +29,16 @@ constexpr int kFixedMinBlocks = PLE_FIXED_MIN_BLOCKS;
 constexpr int kTargetBlocksPerSm = PLE_BLOCKS_PER_SM;
 // Shared-memory budget for the per-head constants of one layer group.
 constexpr int kConstBudgetBytes = 48 * 1024;
+// Batches of at most this many row ids (T * H * L) take the small-batch
+// kernel (one thread per row id); larger ones the tiled kernels.
+#ifndef PLE_SMALL_MAX_ROWS
+#define PLE_SMALL_MAX_ROWS 131072
+#endif
+constexpr int64_t kSmallMaxRows = PLE_SMALL_MAX_ROWS;
+// Threads per block the small-batch kernel aims for (tokens x heads), and
+// its hard maximum (one token of PLE_MAX_HEADS heads).
+constexpr int kSmallBlockThreads = 128;
+constexpr int kSmallMaxThreads = 256;
 
 struct RowIdsParams {
     const void* ids;        // [T] int32 or int64
@@ -69,6 +79,7 @@ struct RowIdsLaunch {
     dim3 grid;
     dim3 block;
     size_t smem_bytes;
+    bool small;  // the small-batch kernel (else a tiled one)
 };
 
 // Per-device facts the launch configuration depends on, cached per device.
@@ -88,6 +99,12 @@ cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaun
 // The tuned (ngram_size, heads_per_ngram) pairs of the fixed-shape kernel.
 bool shape_is_fixed(int N, int hpn);
 cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                                 cudaStream_t stream);
+// The small-batch kernel: whether a batch is small enough, its launch shape,
+// its launch.
+bool small_batch_fits(const RowIdsParams& p);
+RowIdsLaunch plan_small(RowIdsParams& p);
+cudaError_t launch_row_ids_small(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                  cudaStream_t stream);
 
 cudaError_t launch_row_embed(const RowIdsParams& p, const EmbedArgs& e, int id_bytes,

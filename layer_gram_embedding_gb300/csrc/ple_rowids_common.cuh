@@ -237,12 +237,14 @@ __device__ __forceinline__ void carry_context(const RowIdsParams& p, const int64
 }
 
 // Requests with no token in this batch keep their context row.  Needs
-// cu_seqlens; run by the blocks of the first layer group.
+// cu_seqlens; run by the blocks of the first layer group (any block shape).
 template <typename IdT>
 __device__ __forceinline__ void carry_empty_requests(const RowIdsParams& p, int N) {
     if (p.next_ctx == nullptr || p.cu == nullptr || blockIdx.y != 0) return;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.B; r += stride) {
+    const int64_t nthreads = (int64_t)blockDim.x * blockDim.y * blockDim.z;
+    const int64_t tid = threadIdx.x + (int64_t)blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+    const int64_t stride = (int64_t)gridDim.x * nthreads;
+    for (int64_t r = (int64_t)blockIdx.x * nthreads + tid; r < p.B; r += stride) {
         if (__ldg(p.cu + r) == __ldg(p.cu + r + 1)) {
             const IdT* src = static_cast<const IdT*>(p.ctx) + r * (N - 1);
             IdT* dst = static_cast<IdT*>(p.next_ctx) + r * (N - 1);

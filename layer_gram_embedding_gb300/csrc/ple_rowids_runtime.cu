@@ -1,5 +1,6 @@
 // The PLE n-gram row-id hash on sm_103a: the runtime-shape kernel, the launch
-// plan and the dispatch between it and the fixed-shape kernel.
+// plan and the dispatch between it, the fixed-shape kernel and the
+// small-batch kernel (ple_rowids_small.cu).
 //
 // The runtime-shape kernel serves every (ngram_size, heads_per_ngram) the
 // fixed-shape kernel is not compiled for, and the index-free decode: one
@@ -100,7 +101,9 @@ bool shape_is_fixed(int N, int hpn) {
 static bool uses_fixed_kernel(const RowIdsParams& p) { return shape_is_fixed(p.N, p.hpn); }
 
 RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_layout) {
+    if (!runtime_layout && small_batch_fits(p)) return plan_small(p);
     RowIdsLaunch cfg;
+    cfg.small = false;
     const int64_t tiles = (p.T + kTileTokens - 1) / kTileTokens;
     int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
     const bool fixed_shape = !runtime_layout && uses_fixed_kernel(p);
@@ -133,6 +136,7 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
 
 cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                            cudaStream_t stream) {
+    if (cfg.small) return launch_row_ids_small(p, id_bytes, cfg, stream);
     if (uses_fixed_kernel(p)) return launch_row_ids_fixed(p, id_bytes, cfg, stream);
     KernelFn fn;
     if (p.out_bytes == 4)

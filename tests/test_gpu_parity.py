@@ -67,6 +67,27 @@ def assert_same(got: torch.Tensor, expect: np.ndarray, what: str):
 
 WORKLOADS = {b.name + ("_i32" if b.ids.dtype == np.int32 else ""): b for b in wl.all_workloads()}
 
+# The library hashes a call of at most small_batch_max_rows() row ids with
+# the small-batch kernel (one thread per row id) and a larger one with the
+# tiled kernels; the edge-case tests run every case through both.
+KERNELS = ["small", "tiled"]
+
+
+def for_kernel(batch, kernel):
+    """The batch as it is for the small-batch kernel, or, for the tiled
+    kernels, with its layers repeated until the call has more row ids than
+    the small-batch kernel takes.  Repeated layers have the same parameters,
+    so the oracle's rows repeat with them."""
+    limit = ple.small_batch_max_rows()
+    rows = batch.row_ids_per_call
+    if kernel == "small":
+        assert rows <= limit, f"{rows} row ids: more than the small-batch kernel takes"
+        return batch
+    k = limit // rows + 1
+    return dataclasses.replace(batch, layer_multipliers=np.tile(batch.layer_multipliers, (k, 1)),
+                               vocab_sizes=np.tile(batch.vocab_sizes, (k, 1)),
+                               offsets=np.tile(batch.offsets, (k, 1)))
+
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_token_index_matches_oracle(name):
@@ -153,14 +174,16 @@ def test_int32_row_ids_full_size(name):
     assert_same(out, low32(oracle_rows(batch)), f"{name} int32")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("chunk", range(3))
-def test_int32_row_ids_random_edges(chunk):
+def test_int32_row_ids_random_edges(chunk, kernel):
     """Random offsets push row ids past 2^31 (the low words wrap); misaligned
     outputs (4- but not 16-byte aligned) take the scalar stores."""
     for seed in range(chunk * 40, (chunk + 1) * 40):
-        batch = wl.random_batch(9000 + seed, T_max=150,
-                                ids_dtype=np.int32 if seed % 2 else np.int64,
-                                N=[3, 4, 5, 3, 6][seed % 5], hpn=[2, 4, 8, 4, 3][seed % 5])
+        batch = for_kernel(wl.random_batch(9000 + seed, T_max=150,
+                                           ids_dtype=np.int32 if seed % 2 else np.int64,
+                                           N=[3, 4, 5, 3, 6][seed % 5],
+                                           hpn=[2, 4, 8, 4, 3][seed % 5]), kernel)
         req, local = gpu_index(batch)
         L, T, H = batch.num_layers, batch.num_tokens, batch.num_heads
         buf = torch.full((L * T * H + 1,), 77, dtype=torch.int32, device=DEV)
@@ -172,8 +195,9 @@ def test_int32_row_ids_random_edges(chunk):
         assert_same(out, low32(oracle_rows(batch)), f"int32 seed {seed}")
 
 
-def test_int32_row_ids_decode_without_index():
-    batch = wl.decode(8)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_int32_row_ids_decode_without_index(kernel):
+    batch = for_kernel(wl.decode(8), kernel)
     out = ple.ple_row_ids(dev(batch.ids), None, None, dev(batch.ngram_context),
                           dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
                           3, 2, batch.boundary_id, out_dtype=torch.int32)
@@ -214,13 +238,14 @@ def test_context_carry_full_size(name):
         assert_same(nxt, oracle_carry(batch), f"{name} carried context, index-free")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("chunk", range(3))
-def test_context_carry_random_edges(chunk):
+def test_context_carry_random_edges(chunk, kernel):
     """Empty requests keep their row, short requests mix context and tokens,
     int32 ids and int32 row ids."""
     for seed in range(chunk * 50, (chunk + 1) * 50):
-        batch = wl.random_batch(11000 + seed, T_max=120,
-                                ids_dtype=np.int32 if seed % 2 else np.int64)
+        batch = for_kernel(wl.random_batch(11000 + seed, T_max=120,
+                                           ids_dtype=np.int32 if seed % 2 else np.int64), kernel)
         out_dtype = torch.int32 if seed % 3 == 0 else torch.int64
         out, nxt = gpu_rows_carry(batch, out_dtype=out_dtype)
         exp = oracle_rows(batch)
@@ -228,10 +253,11 @@ def test_context_carry_random_edges(chunk):
         assert_same(nxt, oracle_carry(batch), f"carried context {seed}")
 
 
-def test_decode_steps_chain_through_the_carry():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_decode_steps_chain_through_the_carry(kernel):
     """Five decode steps, each fed the context the previous step carried,
     against the oracle run step by step."""
-    b = wl.decode(8)
+    b = for_kernel(wl.decode(8), kernel)
     ctx_o = b.ngram_context.copy()
     ctx_g = dev(b.ngram_context)
     M, vocab, off = dev(b.layer_multipliers), dev(b.vocab_sizes), dev(b.offsets)
@@ -330,35 +356,39 @@ def test_row_embed_large_prefill_sample():
     check_embed(batch, wl.embed_table(rng, 8, 2 ** 16, 64), what="prefill sample")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("chunk", range(6))
-def test_random_edge_batches(chunk):
+def test_random_edge_batches(chunk, kernel):
     """Small ragged batches spanning several 64-token tiles with ragged tails,
     empty requests, decodes, ngram_size 2..8, heads 1..3 per order, 1..3
     layers, boundary densities 0..1, INT64_MIN/MAX multipliers, and vocab
     sizes at the 32-bit edges, negative, tiny and huge."""
     for seed in range(chunk * 60, (chunk + 1) * 60):
         dtype = np.int32 if seed % 3 == 0 else np.int64
-        batch = wl.random_batch(seed, T_max=200, ids_dtype=dtype)
+        batch = for_kernel(wl.random_batch(seed, T_max=200, ids_dtype=dtype), kernel)
         assert_same(gpu_rows(batch), oracle_rows(batch), f"seed {seed}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("N", list(range(9, 17)))
-def test_long_ngrams_generic_path(N):
-    batch = wl.random_batch(5000 + N, N=N, hpn=2, L=2, T_max=150)
+def test_long_ngrams_generic_path(N, kernel):
+    batch = for_kernel(wl.random_batch(5000 + N, N=N, hpn=2, L=2, T_max=150), kernel)
     assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N}")
 
 
 @pytest.mark.parametrize("N,hpn", [(2, 1), (2, 255), (3, 128), (5, 64), (16, 17), (4, 85),
                                    (3, 33), (9, 5)])
-def test_head_counts(N, hpn):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_head_counts(N, hpn, kernel):
     if (N - 1) * hpn > ple.PLE_MAX_HEADS:
         pytest.skip("beyond PLE_MAX_HEADS")
-    batch = wl.random_batch(6000 + N * 1000 + hpn, N=N, hpn=hpn, L=2, T_max=100,
-                            vocab_mode="primes")
+    batch = for_kernel(wl.random_batch(6000 + N * 1000 + hpn, N=N, hpn=hpn, L=2, T_max=100,
+                                       vocab_mode="primes"), kernel)
     assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N} hpn={hpn}")
 
 
-def test_full_range_ids_and_extreme_boundary():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_full_range_ids_and_extreme_boundary(kernel):
     rng = np.random.default_rng(77)
     for b in (wl.I64_MIN, wl.I64_MAX, 0, -1):
         batch = wl.random_batch(int(rng.integers(0, 10 ** 6)), T_max=150, boundary=b)
@@ -366,6 +396,7 @@ def test_full_range_ids_and_extreme_boundary():
                            endpoint=True)
         ids[rng.random(batch.num_tokens) < 0.2] = b
         batch.ids = ids
+        batch = for_kernel(batch, kernel)
         assert_same(gpu_rows(batch), oracle_rows(batch), f"b={b}")
 
 
@@ -426,8 +457,9 @@ def test_per_layer_calls_with_row_pointers():
         assert torch.equal(out, full[l])
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("B", [1, 4, 8, 63, 64, 65, 1000])
-def test_decode_without_an_index(B):
+def test_decode_without_an_index(B, kernel):
     """req = local = NULL: each token its own request at offset 0."""
     batch = wl.decode(min(B, 8)) if B <= 8 else wl.random_batch(7000 + B, decode_batch=True,
                                                                 T_max=B, N=3, hpn=2, L=2)
@@ -436,18 +468,20 @@ def test_decode_without_an_index(B):
         batch.ids = rng.integers(0, wl.VOCAB, size=B, dtype=np.int64)
         batch.ngram_context = rng.integers(0, wl.VOCAB, size=(B, 2), dtype=np.int64)
         batch.ngram_context[rng.random((B, 2)) < 0.3] = batch.boundary_id
+    batch = for_kernel(batch, kernel)
     out = ple.ple_row_ids(dev(batch.ids), None, None, dev(batch.ngram_context),
                           dev(batch.layer_multipliers), dev(batch.vocab_sizes), dev(batch.offsets),
                           batch.ngram_size, batch.heads_per_ngram, batch.boundary_id)
     assert_same(out, oracle_rows(batch), f"index-free decode B={B}")
 
 
-def test_decode_without_an_index_in_a_graph():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_decode_without_an_index_in_a_graph(kernel):
     """One launch per decode step: capture once, replay with fresh ids."""
-    b0 = wl.decode(8)
+    b0 = for_kernel(wl.decode(8), kernel)
     ids, ctx = dev(b0.ids), dev(b0.ngram_context)
     M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
-    out = torch.empty((1, 8, 4), dtype=torch.int64, device=DEV)
+    out = torch.empty((b0.num_layers, 8, 4), dtype=torch.int64, device=DEV)
 
     def step():
         ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, 3, 2, b0.boundary_id, out=out)
@@ -462,7 +496,8 @@ def test_decode_without_an_index_in_a_graph():
     with torch.cuda.graph(g):
         step()
     for replay in (1, 2, 3):
-        fresh = wl.decode(8, replay)
+        fresh = dataclasses.replace(b0, ids=wl.decode(8, replay).ids,
+                                    ngram_context=wl.decode(8, replay).ngram_context)
         ids.copy_(dev(fresh.ids))
         ctx.copy_(dev(fresh.ngram_context))
         g.replay()
@@ -470,19 +505,20 @@ def test_decode_without_an_index_in_a_graph():
         assert_same(out, oracle_rows(fresh), f"index-free replay {replay}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("kind", ["decode_b1", "decode_b4", "decode_b8", "prefill_512"])
-def test_cuda_graph_capture_and_three_replays(kind):
+def test_cuda_graph_capture_and_three_replays(kind, kernel):
     """Capture the index build and the hash once on fixed buffers; replay
     three times with fresh ids and context, each equal to the oracle."""
     make = (lambda r: wl.decode(int(kind[-1]), r)) if kind.startswith("decode") else wl.prefill_512
-    b0 = make(0)
+    b0 = for_kernel(make(0), kernel)
     ids, ctx = dev(b0.ids), dev(b0.ngram_context)
     M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
     cu = dev(b0.cu_seqlens) if b0.cu_seqlens is not None else None
     T, B = b0.num_tokens, b0.num_requests
     req = torch.empty(T, dtype=torch.int32, device=DEV)
     local = torch.empty(T, dtype=torch.int32, device=DEV)
-    out = torch.full((1, T, 4), -123, dtype=torch.int64, device=DEV)
+    out = torch.full((b0.num_layers, T, 4), -123, dtype=torch.int64, device=DEV)
 
     def step():
         ple.ple_build_token_index(cu, B, T, b0.is_decode, req=req, local=local, device=DEV)
@@ -527,12 +563,15 @@ def test_refuses_a_geometry_it_cannot_address(what):
     assert bool((out == 0x5EED).all())
 
 
-def test_out_of_range_index_data_is_clamped_not_read_out_of_bounds():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_out_of_range_index_data_is_clamped_not_read_out_of_bounds(kernel):
     """req outside [0, B) and local outside [0, t] are device data the host
     cannot check; the kernel clamps them (req into [0, B-1], local into
     [0, t]) and stays in bounds.  The rows then follow the page's addressing
-    rule on the clamped values, which the brute force evaluates directly."""
-    batch = wl.random_batch(4242, N=4, hpn=2, L=1, T_max=100, decode_batch=False)
+    rule on the clamped values, which the brute force evaluates directly
+    (on one layer; the tiled case repeats that layer)."""
+    one = wl.random_batch(4242, N=4, hpn=2, L=1, T_max=100, decode_batch=False)
+    batch = for_kernel(one, kernel)
     T, B = batch.num_tokens, batch.num_requests
     oreq, olocal = oracle_index(batch)
     rng = np.random.default_rng(9)
@@ -547,10 +586,22 @@ def test_out_of_range_index_data_is_clamped_not_read_out_of_bounds():
                           dev(batch.offsets), 4, 2, batch.boundary_id)
     creq = np.clip(req, 0, B - 1)
     clocal = np.minimum(np.maximum(local, 0), np.arange(T))
-    exp = np.array(brute_row_ids(batch.ids, creq, clocal, batch.ngram_context,
-                                 batch.layer_multipliers, batch.vocab_sizes, batch.offsets, 4, 2,
-                                 batch.boundary_id), dtype=np.int64)
-    assert_same(out, exp, "clamped index")
+    exp = np.array(brute_row_ids(one.ids, creq, clocal, one.ngram_context,
+                                 one.layer_multipliers, one.vocab_sizes, one.offsets, 4, 2,
+                                 one.boundary_id), dtype=np.int64)
+    assert_same(out, np.tile(exp, (batch.num_layers, 1, 1)), "clamped index")
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_small_and_tiled_kernels_meet_at_the_threshold(extra):
+    """The large prefill's first tokens, as many as the small-batch kernel
+    takes (96 row ids per token) and one token more (the tiled kernels)."""
+    full = wl.prefill_262144()
+    per_token = full.num_layers * full.num_heads
+    T = ple.small_batch_max_rows() // per_token + extra
+    batch = wl.slice_batch(full, 0, T)
+    assert (batch.row_ids_per_call <= ple.small_batch_max_rows()) == (extra == 0)
+    assert_same(gpu_rows(batch), oracle_rows(batch), f"T={T}")
 
 
 def test_floor_mod_routine_matches_cuda_remainder():
