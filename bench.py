@@ -486,7 +486,9 @@ def decode_latency(ple, torch, device):
     """Device µs per call of ple_row_ids at decode B=1: a CUDA graph of 300
     back-to-back calls, median of 7 replays (the page's 7 x 300 method).
     Measured without an index (req = local = NULL, one launch per step) and
-    with a prebuilt index (the page's memoized index)."""
+    with a prebuilt index (the page's memoized index), each with the head
+    constants derived in the call (the page's arguments) and prepared once
+    by ple_prepare_heads (model parameters, fixed across steps)."""
     b = wl.decode(1)
 
     def to_dev(a):
@@ -495,12 +497,17 @@ def decode_latency(ple, torch, device):
     ids, ctx = to_dev(b.ids), to_dev(b.ngram_context)
     M, vocab, off = to_dev(b.layer_multipliers), to_dev(b.vocab_sizes), to_dev(b.offsets)
     req, local = ple.ple_build_token_index(None, 1, 1, True, device=device)
+    heads = ple.ple_prepare_heads(vocab, off)
     out = torch.empty((1, 1, 4), dtype=torch.int64, device=device)
     res = {"launches_per_call": 1, "method": "CUDA graph of 300 calls, median of 7 replays"}
-    for name, (rq, lc) in (("device_us_per_call", (None, None)),
-                           ("device_us_per_call_with_index", (req, local))):
+    for name, (rq, lc, hd) in (("device_us_per_call", (None, None, None)),
+                               ("device_us_per_call_with_index", (req, local, None)),
+                               ("device_us_per_call_prepared_heads", (None, None, heads)),
+                               ("device_us_per_call_with_index_prepared_heads",
+                                (req, local, heads))):
         def call():
-            ple.ple_row_ids(ids, rq, lc, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out)
+            ple.ple_row_ids(ids, rq, lc, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out,
+                            heads=hd)
 
         s = torch.cuda.Stream(device)
         s.wait_stream(torch.cuda.current_stream(device))
@@ -555,6 +562,8 @@ def all_configs(args):
         local = torch.empty(T, dtype=torch.int32, device=device)
         o = torch.empty((L, T, H), dtype=torch.int64, device=device)
         o32 = torch.empty((L, T, H), dtype=torch.int32, device=device)
+        # the row-id variants read a built index, as a serving step would
+        ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
 
         def rows():
             ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
@@ -569,6 +578,12 @@ def all_configs(args):
             ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, batch.ngram_size,
                             batch.heads_per_ngram, batch.boundary_id, out=o)
 
+        heads = ple.ple_prepare_heads(vocab, off)
+
+        def rows_prepared():
+            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
+                            batch.heads_per_ngram, batch.boundary_id, out=o, heads=heads)
+
         def step():
             ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
             rows()
@@ -577,7 +592,8 @@ def all_configs(args):
                "T": T, "B": B, "L": L, "H": H, "ngram_size": batch.ngram_size,
                "row_ids_per_call": batch.row_ids_per_call,
                "algorithmic_bytes": batch.algorithmic_bytes(), "launches_per_call": 1}
-        variants = [("row_ids", rows), ("step", step), ("row_ids_i32", rows_i32)]
+        variants = [("row_ids", rows), ("step", step), ("row_ids_i32", rows_i32),
+                    ("row_ids_prepared_heads", rows_prepared)]
         if batch.is_decode:
             variants.append(("row_ids_no_index", rows_no_index))
         for name, fn in variants:

@@ -53,6 +53,7 @@ typedef enum { PLE_I32 = 0, PLE_I64 = 1 } ple_id_dtype;
 #define PLE_MAX_NGRAM 16   /* largest supported ngram_size */
 #define PLE_MAX_HEADS 256  /* largest supported heads per layer */
 #define PLE_MAX_EMBED_DIM 65536  /* largest supported table row width */
+#define PLE_HEAD_BYTES 48  /* bytes of one head's prepared constants */
 
 /*
  * ple_build_token_index -- per-token (request, offset) index.
@@ -170,8 +171,9 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
                            int32_t* out, void* stream);
 
 /*
- * ple_row_ids_ex -- ple_row_ids with the output dtype chosen and the
- * request contexts carried to the next call, in the same launch.
+ * ple_row_ids_ex -- ple_row_ids with the output dtype chosen, the request
+ * contexts carried to the next call in the same launch, and optionally the
+ * head constants prepared by ple_prepare_heads.
  *
  * The carried context is the state that section "What" (second observation)
  * reads through ngram_context: each request's last ngram_size-1 ids before
@@ -191,9 +193,14 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
  *   next_context  optional [B, ctx_len] output, dtype id_dtype, device; NULL
  *                 for no carry.  Must not overlap ngram_context (the kernel
  *                 reads every context row while it writes).
+ *   heads         optional, device, 16-byte aligned: the constants
+ *                 ple_prepare_heads wrote for these vocab_sizes and offsets.
+ *                 When given, vocab_sizes and offsets are not read (they may
+ *                 be NULL); NULL derives the constants in the call.
  *
- * Errors: as ple_row_ids, plus PLE_ERR_DTYPE for out_dtype and PLE_ERR_NULL
- * for a carry without cu_seqlens outside an index-free decode.
+ * Errors: as ple_row_ids, plus PLE_ERR_DTYPE for out_dtype, PLE_ERR_NULL
+ * for a carry without cu_seqlens outside an index-free decode, and
+ * PLE_ERR_ALIGN for heads not 16-byte aligned.
  */
 ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
                           const int32_t* req, const int32_t* local, const void* ngram_context,
@@ -201,7 +208,34 @@ ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_t
                           const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
                           int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
                           int64_t boundary_id, void* out, int32_t out_dtype,
-                          const int32_t* cu_seqlens, void* next_context, void* stream);
+                          const int32_t* cu_seqlens, void* next_context, const void* heads,
+                          void* stream);
+
+/*
+ * ple_prepare_heads -- each head's remainder constants, computed once.
+ *
+ * Every row id ends with floormod(mix, vocab_sizes[l][h]) + offsets[l][h]
+ * (section "What"; the floored sign rule of section "Why it is safe").  The
+ * kernels do that remainder with a few multiplies by a per-head reciprocal
+ * (Barrett / Granlund-Montgomery), which costs one 64-bit division per head
+ * to set up -- a step of its own on the critical path of a decode call.
+ * vocab_sizes and offsets are model parameters, so a caller that hashes many
+ * batches with the same ones can set the constants up once here and pass
+ * them as `heads` to ple_row_ids_ex.  The row ids are the same either way.
+ * No counterpart on the page: a library-side precomputation.
+ *
+ *   vocab_sizes, offsets  [L, H] int64, device, as ple_row_ids.
+ *   num_layers, num_heads L >= 1, 1 <= H <= PLE_MAX_HEADS.
+ *   heads                 output, device, L * H * PLE_HEAD_BYTES bytes, 16-byte
+ *                         aligned; an opaque layout valid for these
+ *                         parameters only (a later change to vocab_sizes or
+ *                         offsets needs a new call).
+ *
+ * Errors: PLE_ERR_SIZE, PLE_ERR_NULL, PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ * One kernel launch (ordered after earlier work on the stream).
+ */
+ple_status ple_prepare_heads(const int64_t* vocab_sizes, const int64_t* offsets,
+                             int32_t num_layers, int32_t num_heads, void* heads, void* stream);
 
 /*
  * ple_row_embed -- the row ids' table gather, fused with the hash.

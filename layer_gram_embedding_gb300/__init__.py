@@ -8,8 +8,9 @@ never a fallback.
 
 from .binding import (PLE_ERR_ALIGN, PLE_ERR_CUDA, PLE_ERR_DTYPE, PLE_ERR_GEOMETRY_CTX,
                       PLE_ERR_GEOMETRY_HEADS, PLE_ERR_NULL, PLE_ERR_SIZE, PLE_I32, PLE_I64,
-                      PLE_MAX_EMBED_DIM, PLE_MAX_HEADS, PLE_MAX_NGRAM, PLE_OK, PleError, lib,
-                      ple_build_token_index, ple_row_embed, ple_row_ids,
+                      PLE_HEAD_BYTES, PLE_MAX_EMBED_DIM, PLE_MAX_HEADS, PLE_MAX_NGRAM, PLE_OK,
+                      PleError, lib, ple_build_token_index, ple_prepare_heads, ple_row_embed,
+                      ple_row_ids,
                       ple_selftest_floor_mod, ple_validate_index, small_batch_max_rows,
                       status_string)
 
@@ -19,8 +20,9 @@ __all__ = [
     "TokenIndexCache",
     "PLE_OK", "PLE_ERR_NULL", "PLE_ERR_SIZE", "PLE_ERR_GEOMETRY_CTX", "PLE_ERR_GEOMETRY_HEADS",
     "PLE_ERR_DTYPE", "PLE_ERR_ALIGN", "PLE_ERR_CUDA", "PLE_I32", "PLE_I64", "PLE_MAX_NGRAM",
-    "PLE_MAX_HEADS", "PLE_MAX_EMBED_DIM", "PleError", "lib", "status_string",
+    "PLE_MAX_HEADS", "PLE_MAX_EMBED_DIM", "PLE_HEAD_BYTES", "PleError", "lib", "status_string",
     "small_batch_max_rows",
-    "ple_build_token_index", "ple_row_ids", "ple_row_embed", "ple_selftest_floor_mod",
+    "ple_build_token_index", "ple_prepare_heads", "ple_row_ids", "ple_row_embed",
+    "ple_selftest_floor_mod",
     "ple_validate_index",
 ]

@@ -33,6 +33,7 @@ PLE_I64 = 1
 PLE_MAX_NGRAM = 16
 PLE_MAX_HEADS = 256
 PLE_MAX_EMBED_DIM = 65536
+PLE_HEAD_BYTES = 48
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libple.so")
 
@@ -45,7 +46,8 @@ SIGNATURES = {
     "ple_row_ids_i32": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
                                _I32, _I32, _I64, _P, _P]),
     "ple_row_ids_ex": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
-                              _I32, _I32, _I64, _P, _I32, _P, _P, _P]),
+                              _I32, _I32, _I64, _P, _I32, _P, _P, _P, _P]),
+    "ple_prepare_heads": (_I32, [_P, _P, _I32, _I32, _P, _P]),
     "ple_row_embed": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
                              _I32, _I32, _I64, _P, _I64, _I32, _P, _P]),
     "ple_validate_index": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P, _P]),
@@ -173,14 +175,17 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                 vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
                 heads_per_ngram: int, boundary_id: int, out: torch.Tensor | None = None,
                 stream=None, out_dtype=torch.int64, cu_seqlens: torch.Tensor | None = None,
-                next_context: torch.Tensor | None = None) -> torch.Tensor:
+                next_context: torch.Tensor | None = None,
+                heads: torch.Tensor | None = None) -> torch.Tensor:
     """Row ids [L, T, H] int64 (one launch for every layer).
 
     out_dtype=torch.int32 calls ple_row_ids_i32 instead: the low 32 bits of
     each row id, half the output bytes.  next_context ([B, ngram_size-1],
     dtype of the ids, not overlapping ngram_context) receives each request's
     carried context in the same launch (ple_row_ids_ex); it needs cu_seqlens
-    unless req and local are None (index-free decode).
+    unless req and local are None (index-free decode).  heads: the constants
+    ple_prepare_heads made from these vocab_sizes and offsets, read instead
+    of deriving them in the call (ple_row_ids_ex).
 
     input_ids [T] and ngram_context [B, ngram_size-1]: int32 or int64, same
     dtype.  layer_multipliers [L, N] (or [N]), vocab_sizes and offsets
@@ -226,6 +231,11 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
         raise ValueError(f"{where}: offsets must have the shape of vocab_sizes")
     if out_dtype not in (torch.int64, torch.int32):
         raise TypeError(f"{where}: out_dtype must be torch.int64 or torch.int32")
+    if heads is not None:
+        _need(heads, torch.uint8, "heads", where)
+        if tuple(heads.shape) != (L, H, PLE_HEAD_BYTES) or heads.device != dev:
+            raise ValueError(f"{where}: heads must be ple_prepare_heads' [L, H, "
+                             f"{PLE_HEAD_BYTES}] on the ids' device")
     if out is None:
         out = torch.empty((L, T, H), dtype=out_dtype, device=dev)
     else:
@@ -239,22 +249,57 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                   _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx),
                   ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
                   int(heads_per_ngram), L, int(boundary_id), _ptr(out))
-        if next_context is None:
+        if next_context is None and heads is None:
             fn = lib().ple_row_ids if out_dtype == torch.int64 else lib().ple_row_ids_i32
             st = fn(*common, _stream_handle(stream, dev))
         else:
-            if next_context.dtype != input_ids.dtype or tuple(next_context.shape) != tuple(ctx.shape):
-                raise ValueError(f"{where}: next_context must be [B, ngram_size-1] of the ids' dtype")
-            if not next_context.is_contiguous() or next_context.device != dev:
-                raise ValueError(f"{where}: next_context must be contiguous, on the ids' device")
-            if cu_seqlens is not None:
-                _need(cu_seqlens, torch.int32, "cu_seqlens", where)
-                if cu_seqlens.device != dev or cu_seqlens.numel() != ctx.shape[0] + 1:
-                    raise ValueError(f"{where}: cu_seqlens must be [B + 1] on the ids' device")
+            null = ctypes.c_void_p(0)
+            if next_context is not None:
+                if (next_context.dtype != input_ids.dtype
+                        or tuple(next_context.shape) != tuple(ctx.shape)):
+                    raise ValueError(
+                        f"{where}: next_context must be [B, ngram_size-1] of the ids' dtype")
+                if not next_context.is_contiguous() or next_context.device != dev:
+                    raise ValueError(
+                        f"{where}: next_context must be contiguous, on the ids' device")
+                if cu_seqlens is not None:
+                    _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+                    if cu_seqlens.device != dev or cu_seqlens.numel() != ctx.shape[0] + 1:
+                        raise ValueError(
+                            f"{where}: cu_seqlens must be [B + 1] on the ids' device")
             st = lib().ple_row_ids_ex(*common, PLE_I64 if out_dtype == torch.int64 else PLE_I32,
-                                      _ptr(cu_seqlens) if cu_seqlens is not None
-                                      else ctypes.c_void_p(0), _ptr(next_context),
+                                      _ptr(cu_seqlens) if (cu_seqlens is not None and
+                                                           next_context is not None) else null,
+                                      _ptr(next_context) if next_context is not None else null,
+                                      _ptr(heads) if heads is not None else null,
                                       _stream_handle(stream, dev))
+    _check(st, where)
+    return out
+
+
+def ple_prepare_heads(vocab_sizes: torch.Tensor, offsets: torch.Tensor,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """[L, H, PLE_HEAD_BYTES] uint8: each head's remainder constants, set up
+    once for these vocab_sizes and offsets ([L, H] or [H] int64 on a CUDA
+    device) and passed to ple_row_ids(heads=...) call after call."""
+    where = "ple_prepare_heads"
+    dev = _one_cuda_device([t for t in (vocab_sizes, offsets, out) if t is not None], where)
+    vocab = vocab_sizes.reshape(1, -1) if vocab_sizes.dim() == 1 else vocab_sizes
+    off = offsets.reshape(1, -1) if offsets.dim() == 1 else offsets
+    for name, t in (("vocab_sizes", vocab), ("offsets", off)):
+        _need(t, torch.int64, name, where)
+    if off.shape != vocab.shape or vocab.dim() != 2:
+        raise ValueError(f"{where}: vocab_sizes and offsets must be [L, H]")
+    L, H = vocab.shape
+    if out is None:
+        out = torch.empty((L, H, PLE_HEAD_BYTES), dtype=torch.uint8, device=dev)
+    else:
+        _need(out, torch.uint8, "out", where)
+        if tuple(out.shape) != (L, H, PLE_HEAD_BYTES):
+            raise ValueError(f"{where}: out must be [L, H, {PLE_HEAD_BYTES}]")
+    with torch.cuda.device(dev):
+        st = lib().ple_prepare_heads(_ptr(vocab), _ptr(off), L, H, _ptr(out),
+                                     _stream_handle(stream, dev))
     _check(st, where)
     return out
 

@@ -84,7 +84,7 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
                           const int64_t* layer_multipliers, const int64_t* vocab_sizes,
                           const int64_t* offsets, int32_t num_heads, int32_t ngram_size,
                           int32_t heads_per_ngram, int32_t num_layers, int64_t boundary_id,
-                          ple::RowIdsParams* p, bool* empty) {
+                          const void* heads, ple::RowIdsParams* p, bool* empty) {
     *empty = false;
     // sizes first, then the page's two geometry preconditions
     if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
@@ -102,14 +102,15 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     // both index pointers NULL: a decode batch, one token per request at offset 0
     const bool index_free = !req && !local;
     if (index_free && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
+    // prepared head constants replace vocab_sizes and offsets
     if (!input_ids || (!index_free && (!req || !local)) || !ngram_context || !layer_multipliers ||
-        !vocab_sizes || !offsets)
+        (!heads && (!vocab_sizes || !offsets)))
         return PLE_ERR_NULL;
     if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
         !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
-        !aligned(offsets, 8))
+        !aligned(offsets, 8) || !aligned(heads, 16))
         return PLE_ERR_ALIGN;
     p->ids = input_ids;
     p->req = req;
@@ -132,6 +133,7 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     p->out_bytes = 8;
     p->cu = nullptr;
     p->next_ctx = nullptr;
+    p->heads = heads;
     return PLE_OK;
 }
 
@@ -141,13 +143,13 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
                         const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
                         int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
                         int64_t boundary_id, void* out, int out_bytes, const int32_t* cu_seqlens,
-                        void* next_context, void* stream) {
+                        void* next_context, const void* heads, void* stream) {
     ple::RowIdsParams p;
     bool empty = false;
     ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
                                    num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
                                    num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
-                                   &p, &empty);
+                                   heads, &p, &empty);
     if (st != PLE_OK) return st;
     if (out_bytes != 4 && out_bytes != 8) return PLE_ERR_DTYPE;
     if (empty) return PLE_OK;
@@ -188,7 +190,7 @@ extern "C" ple_status ple_row_ids(const void* input_ids, int32_t id_dtype, int64
     return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
                         heads_per_ngram, num_layers, boundary_id, out, 8, nullptr, nullptr,
-                        stream);
+                        nullptr, stream);
 }
 
 extern "C" ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -202,7 +204,7 @@ extern "C" ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, i
     return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
                         heads_per_ngram, num_layers, boundary_id, out, 4, nullptr, nullptr,
-                        stream);
+                        nullptr, stream);
 }
 
 extern "C" ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -214,12 +216,29 @@ extern "C" ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, in
                                      int32_t heads_per_ngram, int32_t num_layers,
                                      int64_t boundary_id, void* out, int32_t out_dtype,
                                      const int32_t* cu_seqlens, void* next_context,
-                                     void* stream) {
+                                     const void* heads, void* stream) {
     const int out_bytes = out_dtype == PLE_I32 ? 4 : out_dtype == PLE_I64 ? 8 : 0;
     return row_ids_impl(input_ids, id_dtype, num_tokens, req, local, ngram_context, num_requests,
                         ctx_len, layer_multipliers, vocab_sizes, offsets, num_heads, ngram_size,
                         heads_per_ngram, num_layers, boundary_id, out, out_bytes, cu_seqlens,
-                        next_context, stream);
+                        next_context, heads, stream);
+}
+
+extern "C" ple_status ple_prepare_heads(const int64_t* vocab_sizes, const int64_t* offsets,
+                                        int32_t num_layers, int32_t num_heads, void* heads,
+                                        void* stream) {
+    if (num_layers < 1 || num_heads < 1 || num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
+    if (!vocab_sizes || !offsets || !heads) return PLE_ERR_NULL;
+    if (!aligned(vocab_sizes, 8) || !aligned(offsets, 8) || !aligned(heads, 16))
+        return PLE_ERR_ALIGN;
+    (void)cudaGetLastError();
+    ple::DeviceFacts dev;
+    cudaError_t e = ple::device_facts(&dev);
+    if (e != cudaSuccess) return cuda_failure(e);
+    e = ple::launch_prepare_heads(vocab_sizes, offsets, (int64_t)num_layers * num_heads, heads,
+                                  dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
 }
 
 extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -236,7 +255,7 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
                                    num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
                                    num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
-                                   &p, &empty);
+                                   nullptr, &p, &empty);
     if (st != PLE_OK) return st;
     if (dim < 8 || dim % 8 != 0 || dim > PLE_MAX_EMBED_DIM || table_rows < 0) return PLE_ERR_SIZE;
     // the table's byte size must fit in 64 bits

@@ -76,6 +76,26 @@ __host__ __device__ __forceinline__ HeadConst make_head_const(int64_t v, int64_t
     return c;
 }
 
+// A head's constants prepared once in global memory (ple_prepare_heads), so
+// that a kernel loads them instead of dividing: three 16-byte words per head,
+// {fast}, {ext}, {off low, off high, 0, 0} (PLE_HEAD_BYTES = 48).
+__device__ __forceinline__ void store_head_const(void* heads, int64_t k, const HeadConst& c) {
+    uint4* h = static_cast<uint4*>(heads) + 3 * k;
+    h[0] = c.fast;
+    h[1] = c.ext;
+    h[2] = make_uint4((uint32_t)(uint64_t)c.off, (uint32_t)((uint64_t)c.off >> 32), 0u, 0u);
+}
+
+__device__ __forceinline__ HeadConst load_head_const(const void* heads, int64_t k) {
+    const uint4* h = static_cast<const uint4*>(heads) + 3 * k;
+    HeadConst c;
+    c.fast = __ldg(h);
+    c.ext = __ldg(h + 1);
+    const uint4 o = __ldg(h + 2);
+    c.off = (int64_t)(((uint64_t)o.y << 32) | o.x);
+    return c;
+}
+
 // The signed mix in offset binary, split into 32-bit words.
 struct OffsetBinary {
     uint32_t lo;

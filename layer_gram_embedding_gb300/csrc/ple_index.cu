@@ -1,5 +1,5 @@
-// The per-token (request, offset) index kernel and the floored-remainder
-// self-test kernel.
+// The per-token (request, offset) index kernel, the head-constant
+// preparation kernel and the floored-remainder self-test kernel.
 //
 // The index is the (req[t], local[t]) pair through which the row-id kernel
 // addresses the carried context (FreeToken PR #338, "perf(ple): fuse the
@@ -149,6 +149,17 @@ selftest_floor_mod_kernel(const int64_t* __restrict__ x, const int64_t* __restri
     }
 }
 
+// One head per thread: the constants the row-id kernels would derive from
+// (vocab, offset) at every call, stored once (three 16-byte words a head).
+__global__ void __launch_bounds__(kIndexThreads)
+prepare_heads_kernel(const int64_t* __restrict__ vocab, const int64_t* __restrict__ offsets,
+                     int64_t n, void* __restrict__ heads) {
+    cudaGridDependencySynchronize();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride)
+        store_head_const(heads, k, make_head_const(vocab[k], offsets[k]));
+}
+
 unsigned grid_for(int64_t n, const DeviceFacts& dev) {
     int64_t blocks = (n + kIndexThreads - 1) / kIndexThreads;
     const int64_t cap = 8 * (int64_t)dev.sm_count;
@@ -201,6 +212,14 @@ cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32
                                   const DeviceFacts& dev, cudaStream_t stream) {
     validate_index_kernel<<<grid_for(T, dev), kIndexThreads, 0, stream>>>(
         cu, B, T, is_decode, req, local, reinterpret_cast<unsigned long long*>(first_bad));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_heads(const int64_t* vocab, const int64_t* offsets, int64_t n,
+                                 void* heads, const DeviceFacts& dev, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(prepare_heads_kernel, grid_for(n, dev), stream, vocab, offsets, n,
+                               heads);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

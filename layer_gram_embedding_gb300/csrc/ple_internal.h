@@ -64,6 +64,7 @@ struct RowIdsParams {
     int32_t out_bytes;      // 8: int64 row ids, 4: their low 32 bits
     const int32_t* cu;      // [B+1] cu_seqlens, for the context carry (NULL: decode)
     void* next_ctx;         // [B, N-1] carried context out, dtype of ids (NULL: none)
+    const void* heads;      // [L, H] prepared head constants (NULL: derive from vocab)
 };
 
 // The table gather fused with the hash: table [L, rows, dim] bfloat16 bits,
@@ -117,6 +118,9 @@ cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t 
 cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                   const int32_t* req, const int32_t* local, int64_t* first_bad,
                                   const DeviceFacts& dev, cudaStream_t stream);
+
+cudaError_t launch_prepare_heads(const int64_t* vocab, const int64_t* offsets, int64_t n,
+                                 void* heads, const DeviceFacts& dev, cudaStream_t stream);
 
 cudaError_t launch_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
                                       int64_t* out_fast, int64_t* out_ref, const DeviceFacts& dev,

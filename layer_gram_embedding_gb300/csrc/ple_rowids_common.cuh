@@ -131,7 +131,8 @@ __device__ __forceinline__ SmemLayout carve_smem(unsigned char* base, int G, int
     return s;
 }
 
-// Block prologue: the layer group's head constants and multipliers.
+// Block prologue: the layer group's head constants (prepared ones loaded,
+// else one reciprocal per head) and multipliers.
 // Returns this thread's vote on whether every head takes the 32-bit fast
 // path; the caller publishes the constants with __syncthreads_and once its
 // own window loads are in flight, so the per-head divisions overlap them.
@@ -140,7 +141,8 @@ __device__ __forceinline__ int load_group_constants(const RowIdsParams& p, const
     int fast = 1;
     for (int i = threadIdx.x; i < gl * H; i += blockDim.x) {
         const int64_t k = (int64_t)l0 * H + i;
-        const HeadConst c = make_head_const(p.vocab[k], p.offsets[k]);
+        const HeadConst c = p.heads != nullptr ? load_head_const(p.heads, k)
+                                               : make_head_const(p.vocab[k], p.offsets[k]);
         sm.fast[i] = c.fast;
         sm.off[i] = c.off;
         sm.ext[i] = c.ext;

@@ -15,8 +15,9 @@
 //     (FreeToken PR #338, "perf(ple): fuse the n-gram row-id hash into one
 //     Triton kernel", section "What", second observation: ids[t-s] while
 //     local[t] >= s, else the carried context row), carries the boundary
-//     predicate over the shifts (first observation), and computes its head's
-//     reciprocal itself, in parallel with the window loads;
+//     predicate over the shifts (first observation), and loads its head's
+//     prepared constants (ple_prepare_heads) or computes the reciprocal
+//     itself, in parallel with the window loads;
 //   - no shared memory, no barrier, one store per thread.
 // The arithmetic is the tiled kernels': the same window rule, the same
 // Barrett remainder (ple_divmod.cuh), so the row ids are identical.
@@ -38,8 +39,11 @@ row_ids_small_kernel(const RowIdsParams p) {
     const int o = threadIdx.y;  // order n = o + 2 folds shifts 0..o+1
     const int h = o * p.hpn + threadIdx.x;
     const int64_t k = (int64_t)l * p.H + h;
-    const int64_t vocab = __ldg(reinterpret_cast<const long long*>(p.vocab) + k);
-    const int64_t off = __ldg(reinterpret_cast<const long long*>(p.offsets) + k);
+    // prepared constants are three loads; otherwise the head's reciprocal is
+    // computed here, in parallel with the window loads
+    const bool prepared = p.heads != nullptr;
+    const int64_t vocab = prepared ? 0 : __ldg(reinterpret_cast<const long long*>(p.vocab) + k);
+    const int64_t off = prepared ? 0 : __ldg(reinterpret_cast<const long long*>(p.offsets) + k);
 
     int32_t r, q;
     if (p.index_free)
@@ -58,7 +62,7 @@ row_ids_small_kernel(const RowIdsParams p) {
         // context index stays inside row r on the second
         w[s] = s <= o + 1 ? (q >= s ? load_id<IdT>(ids, t - s) : load_id<IdT>(crow, -s)) : 0;
     }
-    const HeadConst c = make_head_const(vocab, off);
+    const HeadConst c = prepared ? load_head_const(p.heads, k) : make_head_const(vocab, off);
 
     uint64_t mix = (uint64_t)w[0] * (uint64_t)__ldg(ml);
     bool valid = true;

@@ -475,16 +475,20 @@ def test_decode_without_an_index(B, kernel):
     assert_same(out, oracle_rows(batch), f"index-free decode B={B}")
 
 
+@pytest.mark.parametrize("prepared", [False, True])
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_decode_without_an_index_in_a_graph(kernel):
-    """One launch per decode step: capture once, replay with fresh ids."""
+def test_decode_without_an_index_in_a_graph(kernel, prepared):
+    """One launch per decode step: capture once, replay with fresh ids
+    (with the head constants prepared once before capture, or not)."""
     b0 = for_kernel(wl.decode(8), kernel)
     ids, ctx = dev(b0.ids), dev(b0.ngram_context)
     M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
+    heads = ple.ple_prepare_heads(vocab, off) if prepared else None
     out = torch.empty((b0.num_layers, 8, 4), dtype=torch.int64, device=DEV)
 
     def step():
-        ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, 3, 2, b0.boundary_id, out=out)
+        ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, 3, 2, b0.boundary_id, out=out,
+                        heads=heads)
 
     s = torch.cuda.Stream(DEV)
     s.wait_stream(torch.cuda.current_stream(DEV))
@@ -590,6 +594,66 @@ def test_out_of_range_index_data_is_clamped_not_read_out_of_bounds(kernel):
                                  one.layer_multipliers, one.vocab_sizes, one.offsets, 4, 2,
                                  one.boundary_id), dtype=np.int64)
     assert_same(out, np.tile(exp, (batch.num_layers, 1, 1)), "clamped index")
+
+
+def gpu_rows_prepared(batch, out_dtype=torch.int64, carry=False):
+    heads = ple.ple_prepare_heads(dev(batch.vocab_sizes), dev(batch.offsets))
+    req, local = gpu_index(batch)
+    ctx = dev(batch.ngram_context)
+    nxt = torch.full_like(ctx, -5) if carry else None
+    cu = None
+    if carry:
+        cu = dev(batch.cu_seqlens) if batch.cu_seqlens is not None else dev(
+            np.arange(batch.num_requests + 1, dtype=np.int32))
+    out = ple.ple_row_ids(dev(batch.ids), req, local, ctx, dev(batch.layer_multipliers),
+                          dev(batch.vocab_sizes), dev(batch.offsets), batch.ngram_size,
+                          batch.heads_per_ngram, batch.boundary_id, out_dtype=out_dtype,
+                          cu_seqlens=cu, next_context=nxt, heads=heads)
+    return out, nxt
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_prepared_heads_full_size(name):
+    """Head constants set up once by ple_prepare_heads give the same rows."""
+    batch = WORKLOADS[name]
+    out, _ = gpu_rows_prepared(batch)
+    assert_same(out, oracle_rows(batch), f"{name} prepared heads")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("chunk", range(2))
+def test_prepared_heads_random_edges(chunk, kernel):
+    """Every kind of head (32-bit fast path, the general path at the 2^31 /
+    2^32 edges, negative and zero vocab sizes) through prepared constants,
+    with int32 row ids and the context carry in turn."""
+    for seed in range(chunk * 40, (chunk + 1) * 40):
+        batch = for_kernel(wl.random_batch(13000 + seed, T_max=150,
+                                           ids_dtype=np.int32 if seed % 2 else np.int64), kernel)
+        out_dtype = torch.int32 if seed % 3 == 0 else torch.int64
+        out, nxt = gpu_rows_prepared(batch, out_dtype=out_dtype, carry=seed % 4 == 1)
+        exp = oracle_rows(batch)
+        assert_same(out, low32(exp) if out_dtype == torch.int32 else exp, f"prepared {seed}")
+        if nxt is not None:
+            assert_same(nxt, oracle_carry(batch), f"prepared carry {seed}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prepared_heads_replace_vocab_and_offsets(kernel):
+    """With prepared constants the call reads neither vocab_sizes nor
+    offsets: NULL for both through the C ABI."""
+    batch = for_kernel(wl.random_batch(4711, N=4, hpn=3, L=2, T_max=150), kernel)
+    heads = ple.ple_prepare_heads(dev(batch.vocab_sizes), dev(batch.offsets))
+    req, local = gpu_index(batch)
+    ids, ctx, M = dev(batch.ids), dev(batch.ngram_context), dev(batch.layer_multipliers)
+    L, T, H = batch.num_layers, batch.num_tokens, batch.num_heads
+    out = torch.full((L, T, H), -1, dtype=torch.int64, device=DEV)
+    st = ple.lib().ple_row_ids_ex(ids.data_ptr(), ple.PLE_I64, T, req.data_ptr(),
+                                  local.data_ptr(), ctx.data_ptr(), batch.num_requests, 3,
+                                  M.data_ptr(), None, None, H, 4, 3, L, batch.boundary_id,
+                                  out.data_ptr(), ple.PLE_I64, None, None, heads.data_ptr(),
+                                  torch.cuda.current_stream(DEV).cuda_stream)
+    assert st == ple.PLE_OK
+    assert_same(out, oracle_rows(batch), "prepared heads, no vocab / offsets")
 
 
 @pytest.mark.parametrize("extra", [0, 1])

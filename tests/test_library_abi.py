@@ -102,12 +102,12 @@ def test_row_ids_host_checks(lib, kw, status):
 
 def row_ids_ex(lib, **kw):
     a = dict(ids=A, dtype=1, T=64, req=A, local=A, ctx=A, B=1, ctx_len=2, M=A, vocab=A, off=A,
-             H=4, N=3, hpn=2, L=1, b=7, out=A, out_dtype=1, cu=A, nxt=A)
+             H=4, N=3, hpn=2, L=1, b=7, out=A, out_dtype=1, cu=A, nxt=A, heads=None)
     a.update(kw)
     return lib.ple_row_ids_ex(a["ids"], a["dtype"], a["T"], a["req"], a["local"], a["ctx"],
                               a["B"], a["ctx_len"], a["M"], a["vocab"], a["off"], a["H"], a["N"],
                               a["hpn"], a["L"], a["b"], a["out"], a["out_dtype"], a["cu"],
-                              a["nxt"], None)
+                              a["nxt"], a["heads"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -120,9 +120,29 @@ def row_ids_ex(lib, **kw):
     (dict(out_dtype=0, out=A + 2), ple.PLE_ERR_ALIGN),
     (dict(out_dtype=1, out=A + 4), ple.PLE_ERR_ALIGN),
     (dict(req=None, local=None, cu=None, T=4, B=5), ple.PLE_ERR_SIZE),
+    (dict(heads=A + 8), ple.PLE_ERR_ALIGN),                     # prepared constants: 16 bytes
+    (dict(vocab=None, off=None, out_dtype=2), ple.PLE_ERR_NULL),
+    # with prepared constants vocab_sizes and offsets are not needed: the
+    # call gets past the pointer checks to the output dtype
+    (dict(vocab=None, off=None, heads=A, out_dtype=2), ple.PLE_ERR_DTYPE),
+    (dict(vocab=None, off=None, heads=A, ids=None), ple.PLE_ERR_NULL),
 ])
 def test_row_ids_ex_host_checks(lib, kw, status):
     assert row_ids_ex(lib, **kw) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, 0, 4, A), ple.PLE_ERR_SIZE),
+    ((A, A, 1, 0, A), ple.PLE_ERR_SIZE),
+    ((A, A, 1, 257, A), ple.PLE_ERR_SIZE),
+    ((None, A, 1, 4, A), ple.PLE_ERR_NULL),
+    ((A, None, 1, 4, A), ple.PLE_ERR_NULL),
+    ((A, A, 1, 4, None), ple.PLE_ERR_NULL),
+    ((MIS, A, 1, 4, A), ple.PLE_ERR_ALIGN),
+    ((A, A, 1, 4, A + 8), ple.PLE_ERR_ALIGN),
+])
+def test_prepare_heads_host_checks(lib, args, status):
+    assert lib.ple_prepare_heads(*args, None) == status
 
 
 def row_embed(lib, **kw):
