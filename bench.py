@@ -716,6 +716,8 @@ def main(argv=None):
                     help="layers of the large prefill the gather runs (default all 8)")
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload (graph of 300 calls) instead of the contract line")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the decode B=1 latency (graph of 300 calls), one JSON object")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -725,6 +727,15 @@ def main(argv=None):
         return all_configs(args)
     if args.embed:
         return embed_bench(args)
+    if args.decode_only:
+        import torch
+
+        import layer_gram_embedding_gb300 as ple
+        from layer_gram_embedding_gb300 import build as lib_build
+
+        lib_build.build()
+        print(json.dumps({"decode_b1": decode_latency(ple, torch, torch.device("cuda", 0))}))
+        return 0
     return our_arm(args)
 
 
