@@ -550,6 +550,10 @@ def all_configs(args):
     peaks, _ = measured_peaks()
     out = []
     for batch in wl.all_workloads():
+        wname = batch.name + ("_i32" if batch.ids.dtype == np.int32 else "")
+        if args.only and wname not in args.only:
+            continue
+
         def to_dev(a):
             return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
@@ -588,7 +592,7 @@ def all_configs(args):
             ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
             rows()
 
-        res = {"workload": batch.name + ("_i32" if batch.ids.dtype == np.int32 else ""),
+        res = {"workload": wname,
                "T": T, "B": B, "L": L, "H": H, "ngram_size": batch.ngram_size,
                "row_ids_per_call": batch.row_ids_per_call,
                "algorithmic_bytes": batch.algorithmic_bytes(), "launches_per_call": 1}
@@ -716,6 +720,8 @@ def main(argv=None):
                     help="layers of the large prefill the gather runs (default all 8)")
     ap.add_argument("--all-configs", action="store_true",
                     help="time every workload (graph of 300 calls) instead of the contract line")
+    ap.add_argument("--only", nargs="+", default=None, metavar="WORKLOAD",
+                    help="with --all-configs: only these workloads (e.g. mixed_8192)")
     ap.add_argument("--decode-only", action="store_true",
                     help="only the decode B=1 latency (graph of 300 calls), one JSON object")
     args = ap.parse_args(argv)

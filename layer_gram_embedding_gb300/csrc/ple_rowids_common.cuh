@@ -106,15 +106,27 @@ __host__ __device__ constexpr size_t head_const_bytes(int heads) {
            (size_t)((heads + 3) & ~3) * 4;
 }
 
-// Staging bytes per warp.  Fixed shapes (even heads_per_ngram): 64 rows of
-// 32-bit remainders in 8-byte pairs, odd pitch (H/2 | 1) pairs, or 32 rows of
-// int64 rows with odd pitch (H | 1) for heads off the fast path -- whichever
-// is larger.  Runtime shapes: 32 rows of int64 with odd pitch.
+// Fixed shapes with more heads than this stage half as many tokens at a
+// time (a 32-token half tile on the fast path, a 16-token quarter on the
+// general one), so that shared memory does not cap the resident blocks.
+constexpr int kSplitStageHeads = 16;
+
+__host__ __device__ constexpr int fast_stage_rows(int H) { return H > kSplitStageHeads ? 32 : 64; }
+__host__ __device__ constexpr int general_stage_rows(int H) {
+    return H > kSplitStageHeads ? 16 : 32;
+}
+
+// Staging bytes per warp.  Fixed shapes (even heads_per_ngram): rows of
+// 32-bit remainders in 8-byte pairs, odd pitch (H/2 | 1) pairs, or int64 rows
+// with odd pitch (H | 1) for heads off the fast path -- whichever is larger
+// (row counts above).  Runtime shapes: 32 rows of int64 with odd pitch.
 __host__ __device__ constexpr size_t stage_bytes(int H, bool fixed_shape) {
-    return fixed_shape ? ((size_t)64 * ((H / 2) | 1) * 8 > (size_t)32 * (H | 1) * 8
-                              ? (size_t)64 * ((H / 2) | 1) * 8
-                              : (size_t)32 * (H | 1) * 8)
-                       : (size_t)32 * (H | 1) * 8;
+    return fixed_shape
+               ? ((size_t)fast_stage_rows(H) * ((H / 2) | 1) * 8 >
+                          (size_t)general_stage_rows(H) * (H | 1) * 8
+                      ? (size_t)fast_stage_rows(H) * ((H / 2) | 1) * 8
+                      : (size_t)general_stage_rows(H) * (H | 1) * 8)
+               : (size_t)32 * (H | 1) * 8;
 }
 
 __device__ __forceinline__ SmemLayout carve_smem(unsigned char* base, int G, int H, int N,

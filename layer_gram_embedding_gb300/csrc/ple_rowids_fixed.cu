@@ -77,6 +77,46 @@ __device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int*
     }
 }
 
+// One staged half tile (32 rows) of the split staging, read out for the
+// output type: the head offsets of this lane's columns, then 16-byte stores.
+template <typename OutT, int KU, int P2, int NU, int GU>
+__device__ __forceinline__ void split_readout(const uint2* __restrict__ st, OutT* dst, int lane,
+                                              int nsub, bool vec_out, const int (&soff)[KU],
+                                              const int (&stok)[KU], const SmemLayout& sm,
+                                              int hb, int r0) {
+    if constexpr (sizeof(OutT) == 8) {
+        longlong2 offs[NU];
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            int col = r0 + k * GU;
+            col = col >= KU ? col - KU : col;
+            offs[k] = *reinterpret_cast<const longlong2*>(sm.off + hb + 2 * col);
+        }
+        long long* d = reinterpret_cast<long long*>(dst);
+        if (vec_out && nsub == 32)
+            readout_pairs<KU, P2, NU, GU, true, true>(st, d, lane, 32, soff, stok, offs);
+        else if (vec_out)
+            readout_pairs<KU, P2, NU, GU, true, false>(st, d, lane, nsub, soff, stok, offs);
+        else
+            readout_pairs<KU, P2, NU, GU, false, false>(st, d, lane, nsub, soff, stok, offs);
+    } else {
+        int4 offs[NU];
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+            int col = r0 + k * GU;
+            col = col >= KU ? col - KU : col;
+            offs[k] = *reinterpret_cast<const int4*>(sm.off32 + hb + 4 * col);
+        }
+        int* d = reinterpret_cast<int*>(dst);
+        if (vec_out && nsub == 32)
+            readout_quads<KU, P2, NU, GU, true, true>(st, d, lane, 32, soff, stok, offs);
+        else if (vec_out)
+            readout_quads<KU, P2, NU, GU, true, false>(st, d, lane, nsub, soff, stok, offs);
+        else
+            readout_quads<KU, P2, NU, GU, false, false>(st, d, lane, nsub, soff, stok, offs);
+    }
+}
+
 template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, bool kIndexFree>
 __global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_fixed_kernel(const RowIdsParams p) {
@@ -126,22 +166,31 @@ row_ids_fixed_kernel(const RowIdsParams p) {
 
     if (!all_fast) {
         // some head of this group is off the fast path: int64 rows, 8-byte
-        // readout, one half tile at a time
+        // readout, RG tokens at a time (a half tile, or a quarter when the
+        // staging is split)
+        constexpr int RG = general_stage_rows(H);
         int64_t* st = reinterpret_cast<int64_t*>(stage);
 #pragma unroll 1
         for (int u = 0; u < 2; ++u) {
             const int nsub = u == 0 ? nA : nB;
-            if (nsub <= 0) break;
 #pragma unroll 1
-            for (int l = 0; l < gl; ++l) {
-                const int hb = l * H;
-                hash_layer<N, N, false>(u == 0 ? VA : VB, N, HPT, sm.mul + l * N, sm.fast + hb,
-                                        sm.off + hb, sm.ext + hb, st + lane * PG);
-                __syncwarp();
-                OutT* dst = static_cast<OutT*>(p.out) +
-                            ((int64_t)(l0 + l) * p.T + t0 + 32 * u) * H;
-                readout_runtime<OutT>(st, dst, lane, nsub, H, PG);
-                __syncwarp();
+            for (int q0 = 0; q0 < 32; q0 += RG) {
+                const int nq = min(RG, nsub - q0);
+                if (nq <= 0) break;
+                const bool mine = RG == 32 || (lane >= q0 && lane < q0 + RG);
+#pragma unroll 1
+                for (int l = 0; l < gl; ++l) {
+                    const int hb = l * H;
+                    if (mine)
+                        hash_layer<N, N, false>(u == 0 ? VA : VB, N, HPT, sm.mul + l * N,
+                                                sm.fast + hb, sm.off + hb, sm.ext + hb,
+                                                st + (lane - q0) * PG);
+                    __syncwarp();
+                    OutT* dst = static_cast<OutT*>(p.out) +
+                                ((int64_t)(l0 + l) * p.T + t0 + 32 * u + q0) * H;
+                    readout_runtime<OutT>(st, dst, lane, nq, H, PG);
+                    __syncwarp();
+                }
             }
         }
         return;
@@ -171,6 +220,41 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     }
     const bool full = nA == 32 && nB == 32;
     const bool vec_out = p.out_vec_ok != 0;
+
+    if constexpr (fast_stage_rows(H) == 32) {
+        // split staging: hash and read out one half tile at a time
+#pragma unroll 1
+        for (int l = 0; l < gl; ++l) {
+            const int64_t* ml = sm.mul + l * N;
+            const uint4* hf = sm.fast + l * H;
+            OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
+#pragma unroll 1
+            for (int u = 0; u < 2; ++u) {
+                const int nsub = u == 0 ? nA : nB;
+                if (nsub <= 0) break;
+                // select element by element: the windows stay in registers
+                uint64_t mix = (uint64_t)(u == 0 ? VA[0] : VB[0]) * (uint64_t)ml[0];
+#pragma unroll
+                for (int s = 1; s < N; ++s) {
+                    mix ^= (uint64_t)(u == 0 ? VA[s] : VB[s]) * (uint64_t)ml[s];
+                    const OffsetBinary uu = offset_binary(mix);
+#pragma unroll
+                    for (int j = 0; j < HPT; j += 2) {
+                        const int h = (s - 1) * HPT + j;
+                        const uint4 c0 = hf[h];
+                        const uint4 c1 = hf[h + 1];
+                        stAw[lane * P2 + h / 2] = make_uint2(floormod_fast(uu, c0, c0.z << 1),
+                                                             floormod_fast(uu, c1, c1.z << 1));
+                    }
+                }
+                __syncwarp();
+                split_readout<OutT, KU, P2, NU, GU>(stA, dst + 32 * u * H, lane, nsub, vec_out,
+                                                    soff, stok, sm, l * H, r0);
+                __syncwarp();
+            }
+        }
+        return;
+    }
 
 #pragma unroll 1
     for (int l = 0; l < gl; ++l) {

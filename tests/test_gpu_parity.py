@@ -370,6 +370,21 @@ def test_random_edge_batches(chunk, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("N,hpn", [(3, 2), (3, 4), (4, 4), (5, 8)])
+def test_fixed_shapes_random_edges(N, hpn, kernel):
+    """The tuned shapes with ragged tiles, empty requests, boundary densities
+    0..1 and every kind of vocab size (so both the 32-bit fast path and the
+    general path, whose staging the 32-head shape splits), int64 row ids."""
+    for seed in range(30):
+        dtype = np.int32 if seed % 2 else np.int64
+        batch = for_kernel(wl.random_batch(15000 + 100 * N + 10 * hpn + seed, N=N, hpn=hpn,
+                                           T_max=200, ids_dtype=dtype,
+                                           vocab_mode="primes" if seed % 3 == 0 else "mixed"),
+                           kernel)
+        assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N} hpn={hpn} seed {seed}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("N", list(range(9, 17)))
 def test_long_ngrams_generic_path(N, kernel):
     batch = for_kernel(wl.random_batch(5000 + N, N=N, hpn=2, L=2, T_max=150), kernel)
