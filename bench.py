@@ -3,19 +3,22 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
-one batch: the per-token index build (ple_build_token_index) and the row-id
-hash of every layer (ple_row_ids), two launches, through the C ABI.  The
+one batch, through the C ABI: each token's (request, offset) found from
+cu_seqlens and the row-id hash of every layer, in one launch
+(ple_row_ids_ex with req = local = NULL and cu_seqlens).  The same step as
+two launches -- ple_build_token_index writing the index, then ple_row_ids
+reading it -- is timed beside it.  The
 workload is the large prefill: T=262144 tokens in 4 requests, ngram_size 4,
 4 heads per order (12 heads), 8 layers, int64 ids, 20% adversarial boundary
 runs.  Inputs are resident in HBM before the timed region; 64 distinct input
 sets rotate (256 MiB of inputs) and two output buffers alternate (201 MB of
 row ids written per step), so no step finds its inputs in the 126 MB L2.
 
-Also measured, as extra keys: the row-id kernel's own duration (CUDA events
-around it on its stream) against the HBM roofline, the end-to-end rate with
-host buffers (pinned H2D of ids / cu_seqlens / context, the two calls, D2H of
-all row ids), the decode B=1 device time per call (a CUDA graph of 300 calls,
-median of 7 replays), and the CPU oracle on the host cores.
+Also measured, as extra keys: the row-id kernel's duration (the step's one
+launch, CUDA events on its stream) against the HBM roofline, the end-to-end
+rate with host buffers (pinned H2D of ids / cu_seqlens / context, the call,
+D2H of all row ids), the decode B=1 device time per call (a CUDA graph of 300
+calls, median of 7 replays), and the CPU oracle on the host cores.
 
 --impl reference times the CPU oracle (the only reference this path has) on
 bounded samples of the same workload.
@@ -303,7 +306,7 @@ def our_arm(args):
                          local=torch.empty(T, dtype=torch.int32, device=device)))
     outs = [torch.empty((L, T, H), dtype=torch.int64, device=device) for _ in range(2)]
     P = ctypes.c_void_p
-    idx_args, row_args = [], []
+    idx_args, row_args, search_args = [], [], []
     for k, s in enumerate(sets):
         idx_args.append((P(s["cu"].data_ptr()), B, T, 0, P(s["req"].data_ptr()),
                          P(s["local"].data_ptr()), sh))
@@ -311,17 +314,24 @@ def our_arm(args):
                          P(s["local"].data_ptr()), P(s["ctx"].data_ptr()), B, N - 1,
                          P(M.data_ptr()), P(vocab.data_ptr()), P(off.data_ptr()), H, N, hpn, L,
                          base.boundary_id, P(outs[k % 2].data_ptr()), sh))
-    f_idx, f_rows = lib.ple_build_token_index, lib.ple_row_ids
+        # the whole step in one launch: req = local = NULL with cu_seqlens,
+        # each token's request found in the kernel
+        search_args.append((P(s["ids"].data_ptr()), ple.PLE_I64, T, None, None,
+                            P(s["ctx"].data_ptr()), B, N - 1, P(M.data_ptr()),
+                            P(vocab.data_ptr()), P(off.data_ptr()), H, N, hpn, L,
+                            base.boundary_id, P(outs[k % 2].data_ptr()), ple.PLE_I64,
+                            P(s["cu"].data_ptr()), None, None, sh))
+    f_idx, f_rows, f_search = lib.ple_build_token_index, lib.ple_row_ids, lib.ple_row_ids_ex
 
     def step(i):
+        if f_search(*search_args[i % ROTATE]):
+            raise RuntimeError("library call failed")
+
+    def step_with_index(i):
         k = i % ROTATE
         st = f_idx(*idx_args[k]) | f_rows(*row_args[k])
         if st:
             raise RuntimeError(f"library call failed: status {st}")
-
-    def rows_only(i):
-        if f_rows(*row_args[i % ROTATE]):
-            raise RuntimeError("library call failed")
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     clocks = ClockSampler(visible.split(",")[dist.local_rank].strip() if visible else
@@ -329,6 +339,7 @@ def our_arm(args):
     clocks.start()
     for i in range(args.warmup):
         step(i)
+        step_with_index(i)
     torch.cuda.synchronize(device)
 
     # ---- the timed region: K steps back to back, events only at its ends
@@ -345,36 +356,42 @@ def our_arm(args):
     dist.barrier()
     total_ms = t_start.elapsed_time(t_end)
 
-    # ---- the dominant kernel alone: K launches back to back on the same
-    # stream, events at the ends of the run (an event between launches would
-    # serialise them and add its own drain-and-launch gap to every launch)
-    k_start = torch.cuda.Event(enable_timing=True)
-    k_end = torch.cuda.Event(enable_timing=True)
+    # ---- the step as two launches (ple_build_token_index, then ple_row_ids
+    # reading the index), K steps back to back, for comparison
+    w_start = torch.cuda.Event(enable_timing=True)
+    w_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(device)
-    k_start.record(stream)
+    w_start.record(stream)
     for i in range(args.steps):
-        rows_only(args.warmup + i)
-    k_end.record(stream)
+        step_with_index(args.warmup + i)
+    w_end.record(stream)
     torch.cuda.synchronize(device)
-    kern_avg_ms = k_start.elapsed_time(k_end) / args.steps
-    # the same kernel with an event pair around every launch, for reference
+    with_index_ms = w_start.elapsed_time(w_end) / args.steps
+    # the step's one kernel with an event pair around every launch, for
+    # reference (an event between launches serialises them and adds its own
+    # drain-and-launch gap to every launch)
     n_br = min(args.steps, 200)
     br = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_br)]
     for i in range(n_br):
         br[i][0].record(stream)
-        rows_only(i)
+        step(i)
         br[i][1].record(stream)
     torch.cuda.synchronize(device)
     clocks.mark_off()
     bracketed_ms = float(np.median([a.elapsed_time(b) for a, b in br]))
+    # the step is one launch, so the dominant kernel's average duration is the
+    # step's, measured over the timed region on the launching stream
+    kern_avg_ms = total_ms / args.steps
     total_ms = dist.max(total_ms, device)
     clk = clocks.stop()
 
     rows_per_step = base.row_ids_per_call
     value = dist.world * rows_per_step * args.steps / (total_ms / 1e3)
     idb = base.ids.dtype.itemsize
-    kernel_bytes = T * (idb + 8 + 8 * L * H) + B * (N - 1) * idb + 8 * L * (N + 2 * H)
+    # ids and cu_seqlens read, context and parameters read, row ids written
+    kernel_bytes = (T * (idb + 8 * L * H) + 4 * (B + 1) + B * (N - 1) * idb +
+                    8 * L * (N + 2 * H))
     peaks, peak_kind = measured_peaks()
     achieved = kernel_bytes / (kern_avg_ms / 1e3) / 1e9
     traffic = None
@@ -387,11 +404,12 @@ def our_arm(args):
         pass
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "ple row_ids kernel (row_ids_fixed_kernel<int64, 4, 4>)",
+                "kernel": "ple row_ids kernel (row_ids_fixed_kernel<int64, 4, 4>, requests "
+                          "found from cu_seqlens in the kernel)",
                 "algorithmic_bytes_per_launch": kernel_bytes,
                 "kernel_ms_avg": kern_avg_ms,
-                "kernel_timing": f"{args.steps} back-to-back launches, CUDA events at the ends "
-                                 "of the run, on the launching stream",
+                "kernel_timing": f"the timed region: {args.steps} one-launch steps back to back, "
+                                 "CUDA events at its ends, on the launching stream",
                 "kernel_ms_bracketed_median": bracketed_ms,
                 "peak_kind": peak_kind}
 
@@ -423,8 +441,12 @@ def our_arm(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
-        "gpu_launches_kernel_timing": args.steps + n_br,
+        "gpu_launches": args.steps,
+        "step": "one launch: ple_row_ids_ex with req = local = NULL and cu_seqlens",
+        "step_with_index_build": {
+            "launches": 2, "ms_per_step": with_index_ms,
+            "value": dist.world * rows_per_step / (with_index_ms / 1e3), "unit": UNIT,
+            "what": "ple_build_token_index then ple_row_ids reading the index, back to back"},
         "clocks": clk,
         "decode_b1": decode,
     }
@@ -435,10 +457,10 @@ def our_arm(args):
 
 
 def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
-    """The same metric through ple_build_token_index / ple_row_ids (the Python
-    binding) with host buffers: every step copies its ids, cu_seqlens and
-    context from pinned host memory, runs both calls, and copies every row id
-    back to pinned host memory."""
+    """The same metric through ple_row_ids (the Python binding; requests
+    found from cu_seqlens in the kernel) with host buffers: every step copies
+    its ids, cu_seqlens and context from pinned host memory, runs the call,
+    and copies every row id back to pinned host memory."""
     b0 = batches[0]
     T, B, L, H = b0.num_tokens, b0.num_requests, b0.num_layers, b0.num_heads
     host = []
@@ -449,8 +471,6 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
     d_ids = torch.empty(T, dtype=torch.int64, device=device)
     d_cu = torch.empty(B + 1, dtype=torch.int32, device=device)
     d_ctx = torch.empty((B, b0.ngram_size - 1), dtype=torch.int64, device=device)
-    req = torch.empty(T, dtype=torch.int32, device=device)
-    local = torch.empty(T, dtype=torch.int32, device=device)
     out = torch.empty((L, T, H), dtype=torch.int64, device=device)
     h_out = torch.empty((L, T, H), dtype=torch.int64).pin_memory()
     steps = max(3, min(args.steps, 100))
@@ -462,9 +482,8 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
         d_ids.copy_(h["ids"], non_blocking=True)
         d_cu.copy_(h["cu"], non_blocking=True)
         d_ctx.copy_(h["ctx"], non_blocking=True)
-        ple.ple_build_token_index(d_cu, B, T, False, req=req, local=local)
-        ple.ple_row_ids(d_ids, req, local, d_ctx, M, vocab, off, b0.ngram_size,
-                        b0.heads_per_ngram, b0.boundary_id, out=out)
+        ple.ple_row_ids(d_ids, None, None, d_ctx, M, vocab, off, b0.ngram_size,
+                        b0.heads_per_ngram, b0.boundary_id, out=out, cu_seqlens=d_cu)
         h_out.copy_(out, non_blocking=True)
 
     for i in range(3):

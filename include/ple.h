@@ -171,9 +171,19 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
                            int32_t* out, void* stream);
 
 /*
- * ple_row_ids_ex -- ple_row_ids with the output dtype chosen, the request
- * contexts carried to the next call in the same launch, and optionally the
- * head constants prepared by ple_prepare_heads.
+ * ple_row_ids_ex -- ple_row_ids with the output dtype chosen, the token
+ * index optionally found in the kernel from cu_seqlens, the request contexts
+ * carried to the next call in the same launch, and optionally the head
+ * constants prepared by ple_prepare_heads.
+ *
+ * With req = local = NULL and cu_seqlens given, the kernel finds each
+ * token's request itself: the request r with cu_seqlens[r] <= t <
+ * cu_seqlens[r+1] (a binary search; empty requests own no token), at offset
+ * t - cu_seqlens[r] -- the index ple_build_token_index would build, so a
+ * prefill step is one launch and reads no index.  cu_seqlens must then
+ * describe the batch as ple_build_token_index requires (device data, not
+ * checked; other contents give unspecified rows, never an out-of-bounds
+ * access).
  *
  * The carried context is the state that section "What" (second observation)
  * reads through ngram_context: each request's last ngram_size-1 ids before
@@ -182,14 +192,18 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
  * what the request's next prefill chunk or decode step passes as its
  * ngram_context.  A request with no token in the batch keeps its row.
  *
- *   all arguments up to boundary_id: as ple_row_ids.
+ *   all arguments up to boundary_id: as ple_row_ids, except that req = local
+ *                 = NULL with cu_seqlens given takes any B >= 1 (above).  With
+ *                 req = local = NULL and no cu_seqlens: a decode batch, as in
+ *                 ple_row_ids.
  *   out           [L, T, H] int64 (out_dtype PLE_I64) or int32 (PLE_I32, the
  *                 low 32 bits as in ple_row_ids_i32), aligned to its element.
  *   out_dtype     PLE_I64 or PLE_I32 (else PLE_ERR_DTYPE).
- *   cu_seqlens    [B+1] int32, device, the batch layout the index was built
- *                 from.  Required with next_context unless req = local = NULL
- *                 (index-free decode, where every token ends its request);
- *                 ignored without next_context.
+ *   cu_seqlens    [B+1] int32, device, 4-byte aligned: the batch layout.
+ *                 With req and local: the layout the index was built from,
+ *                 required with next_context and otherwise not read.  Without
+ *                 them: the layout the kernel searches (above); NULL there
+ *                 means a decode batch, where every token ends its request.
  *   next_context  optional [B, ctx_len] output, dtype id_dtype, device; NULL
  *                 for no carry.  Must not overlap ngram_context (the kernel
  *                 reads every context row while it writes).
@@ -199,8 +213,8 @@ ple_status ple_row_ids_i32(const void* input_ids, int32_t id_dtype, int64_t num_
  *                 be NULL); NULL derives the constants in the call.
  *
  * Errors: as ple_row_ids, plus PLE_ERR_DTYPE for out_dtype, PLE_ERR_NULL
- * for a carry without cu_seqlens outside an index-free decode, and
- * PLE_ERR_ALIGN for heads not 16-byte aligned.
+ * for a carry with req and local but without cu_seqlens, and PLE_ERR_ALIGN
+ * for heads not 16-byte aligned or cu_seqlens not 4-byte aligned.
  */
 ple_status ple_row_ids_ex(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
                           const int32_t* req, const int32_t* local, const void* ngram_context,

@@ -182,24 +182,27 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
     out_dtype=torch.int32 calls ple_row_ids_i32 instead: the low 32 bits of
     each row id, half the output bytes.  next_context ([B, ngram_size-1],
     dtype of the ids, not overlapping ngram_context) receives each request's
-    carried context in the same launch (ple_row_ids_ex); it needs cu_seqlens
-    unless req and local are None (index-free decode).  heads: the constants
-    ple_prepare_heads made from these vocab_sizes and offsets, read instead
-    of deriving them in the call (ple_row_ids_ex).
+    carried context in the same launch (ple_row_ids_ex); with req and local
+    it needs cu_seqlens.  req = local = None with cu_seqlens ([B+1] int32):
+    the kernel finds each token's request by searching cu_seqlens, so no
+    index is built or read.  heads: the constants ple_prepare_heads made from
+    these vocab_sizes and offsets, read instead of deriving them in the call
+    (ple_row_ids_ex).
 
     input_ids [T] and ngram_context [B, ngram_size-1]: int32 or int64, same
     dtype.  layer_multipliers [L, N] (or [N]), vocab_sizes and offsets
     [L, H] (or [H]): int64.  out: optional fixed [L, T, H] int64 destination
     (a graph replay then writes into a stable buffer).  req and local both
     None: a decode batch (one token per request at offset 0, B == T), with no
-    index to build or read.  ValueError on the two geometry preconditions and
-    on tensors not all on one CUDA device.
+    index to build or read (without cu_seqlens).  ValueError on the two
+    geometry preconditions and on tensors not all on one CUDA device.
     """
     where = "ple_row_ids"
     if (req is None) != (local is None):
         raise ValueError(f"{where}: pass both req and local, or neither (decode)")
     dev = _one_cuda_device([t for t in (input_ids, req, local, ngram_context, layer_multipliers,
-                                        vocab_sizes, offsets, out) if t is not None], where)
+                                        vocab_sizes, offsets, out, cu_seqlens, next_context,
+                                        heads) if t is not None], where)
     if input_ids.dtype not in (torch.int32, torch.int64):
         raise TypeError(f"{where}: input_ids must be int32 or int64")
     if ngram_context.dtype != input_ids.dtype:
@@ -249,7 +252,10 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                   _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx),
                   ctx.shape[0], ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, N,
                   int(heads_per_ngram), L, int(boundary_id), _ptr(out))
-        if next_context is None and heads is None:
+        # cu_seqlens matters to the kernel for the carry and for the search
+        # mode (no index); otherwise it is not passed
+        use_cu = cu_seqlens is not None and (next_context is not None or req is None)
+        if next_context is None and heads is None and not use_cu:
             fn = lib().ple_row_ids if out_dtype == torch.int64 else lib().ple_row_ids_i32
             st = fn(*common, _stream_handle(stream, dev))
         else:
@@ -262,14 +268,12 @@ def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.
                 if not next_context.is_contiguous() or next_context.device != dev:
                     raise ValueError(
                         f"{where}: next_context must be contiguous, on the ids' device")
-                if cu_seqlens is not None:
-                    _need(cu_seqlens, torch.int32, "cu_seqlens", where)
-                    if cu_seqlens.device != dev or cu_seqlens.numel() != ctx.shape[0] + 1:
-                        raise ValueError(
-                            f"{where}: cu_seqlens must be [B + 1] on the ids' device")
+            if use_cu:
+                _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+                if cu_seqlens.device != dev or cu_seqlens.numel() != ctx.shape[0] + 1:
+                    raise ValueError(f"{where}: cu_seqlens must be [B + 1] on the ids' device")
             st = lib().ple_row_ids_ex(*common, PLE_I64 if out_dtype == torch.int64 else PLE_I32,
-                                      _ptr(cu_seqlens) if (cu_seqlens is not None and
-                                                           next_context is not None) else null,
+                                      _ptr(cu_seqlens) if use_cu else null,
                                       _ptr(next_context) if next_context is not None else null,
                                       _ptr(heads) if heads is not None else null,
                                       _stream_handle(stream, dev))

@@ -84,7 +84,8 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
                           const int64_t* layer_multipliers, const int64_t* vocab_sizes,
                           const int64_t* offsets, int32_t num_heads, int32_t ngram_size,
                           int32_t heads_per_ngram, int32_t num_layers, int64_t boundary_id,
-                          const void* heads, ple::RowIdsParams* p, bool* empty) {
+                          const int32_t* cu_seqlens, const void* heads, ple::RowIdsParams* p,
+                          bool* empty) {
     *empty = false;
     // sizes first, then the page's two geometry preconditions
     if (ngram_size < 2 || ngram_size > PLE_MAX_NGRAM || heads_per_ngram < 1 || num_layers < 1 ||
@@ -99,9 +100,13 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
         return PLE_OK;
     }
     if (num_requests < 1) return PLE_ERR_SIZE;
-    // both index pointers NULL: a decode batch, one token per request at offset 0
+    // both index pointers NULL: the kernel finds each token's request itself,
+    // by searching cu_seqlens when given, else as a decode batch (one token
+    // per request at offset 0)
     const bool index_free = !req && !local;
-    if (index_free && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
+    const int32_t mode = !index_free ? ple::kIdxArrays
+                                     : (cu_seqlens ? ple::kIdxCu : ple::kIdxDecode);
+    if (mode == ple::kIdxDecode && (int64_t)num_requests != num_tokens) return PLE_ERR_SIZE;
     // prepared head constants replace vocab_sizes and offsets
     if (!input_ids || (!index_free && (!req || !local)) || !ngram_context || !layer_multipliers ||
         (!heads && (!vocab_sizes || !offsets)))
@@ -110,7 +115,7 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) || !aligned(req, 4) ||
         !aligned(local, 4) || !aligned(layer_multipliers, 8) || !aligned(vocab_sizes, 8) ||
-        !aligned(offsets, 8) || !aligned(heads, 16))
+        !aligned(offsets, 8) || !aligned(heads, 16) || !aligned(cu_seqlens, 4))
         return PLE_ERR_ALIGN;
     p->ids = input_ids;
     p->req = req;
@@ -129,9 +134,9 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     p->L = num_layers;
     p->ids_vec_ok = aligned(input_ids, 16) ? 1 : 0;
     p->out_vec_ok = 0;
-    p->index_free = index_free ? 1 : 0;
+    p->index_mode = mode;
     p->out_bytes = 8;
-    p->cu = nullptr;
+    p->cu = cu_seqlens;
     p->next_ctx = nullptr;
     p->heads = heads;
     return PLE_OK;
@@ -149,17 +154,16 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
                                    num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
                                    num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
-                                   heads, &p, &empty);
+                                   cu_seqlens, heads, &p, &empty);
     if (st != PLE_OK) return st;
     if (out_bytes != 4 && out_bytes != 8) return PLE_ERR_DTYPE;
     if (empty) return PLE_OK;
     if (!out) return PLE_ERR_NULL;
     // the carry finds each request's last token (and empty requests) through
-    // cu_seqlens, except in an index-free decode
-    if (next_context && !p.index_free && !cu_seqlens) return PLE_ERR_NULL;
+    // cu_seqlens, except in a decode without an index
+    if (next_context && p.index_mode == ple::kIdxArrays && !cu_seqlens) return PLE_ERR_NULL;
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
-    if (!aligned(out, out_bytes) || !aligned(cu_seqlens, 4) || !aligned(next_context, id_bytes))
-        return PLE_ERR_ALIGN;
+    if (!aligned(out, out_bytes) || !aligned(next_context, id_bytes)) return PLE_ERR_ALIGN;
 
     (void)cudaGetLastError();
     ple::DeviceFacts dev;
@@ -168,7 +172,6 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     p.out = out;
     p.out_vec_ok = aligned(out, 16) ? 1 : 0;
     p.out_bytes = out_bytes;
-    p.cu = next_context ? cu_seqlens : nullptr;
     p.next_ctx = next_context;
     const ple::RowIdsLaunch cfg = ple::plan_row_ids(p, dev);
     if (cfg.grid.y > 65535u) return PLE_ERR_SIZE;
@@ -255,7 +258,7 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
                                    num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
                                    num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
-                                   nullptr, &p, &empty);
+                                   nullptr, nullptr, &p, &empty);
     if (st != PLE_OK) return st;
     if (dim < 8 || dim % 8 != 0 || dim > PLE_MAX_EMBED_DIM || table_rows < 0) return PLE_ERR_SIZE;
     // the table's byte size must fit in 64 bits

@@ -40,6 +40,12 @@ constexpr int64_t kSmallMaxRows = PLE_SMALL_MAX_ROWS;
 constexpr int kSmallBlockThreads = 128;
 constexpr int kSmallMaxThreads = 256;
 
+// How the kernels find each token's (request, offset):
+//   kIdxArrays  read req[t], local[t] (an index built by ple_build_token_index)
+//   kIdxDecode  a decode batch: req = t, local = 0, nothing read
+//   kIdxCu      search cu_seqlens for the request owning t, local = t - start
+enum IndexMode : int32_t { kIdxArrays = 0, kIdxDecode = 1, kIdxCu = 2 };
+
 struct RowIdsParams {
     const void* ids;        // [T] int32 or int64
     const int32_t* req;     // [T]
@@ -60,9 +66,9 @@ struct RowIdsParams {
     int32_t stage_pitch;    // row pitch (in int64) of the output staging tile
     int32_t ids_vec_ok;     // ids pointer is 16-byte aligned
     int32_t out_vec_ok;     // out pointer is 16-byte aligned
-    int32_t index_free;     // decode without an index: req[t] = t, local[t] = 0
+    int32_t index_mode;     // IndexMode
     int32_t out_bytes;      // 8: int64 row ids, 4: their low 32 bits
-    const int32_t* cu;      // [B+1] cu_seqlens, for the context carry (NULL: decode)
+    const int32_t* cu;      // [B+1] cu_seqlens: kIdxCu and the context carry (NULL: none)
     void* next_ctx;         // [B, N-1] carried context out, dtype of ids (NULL: none)
     const void* heads;      // [L, H] prepared head constants (NULL: derive from vocab)
 };

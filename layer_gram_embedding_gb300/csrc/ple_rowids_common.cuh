@@ -61,28 +61,6 @@ __device__ __forceinline__ int64_t load_id<int32_t>(const int32_t* p, int64_t i)
     return (int64_t)__ldg(p + i);
 }
 
-// A full 64-token tile of ids, 16-byte vector loads (tile base 16B-aligned).
-template <typename IdT>
-__device__ __forceinline__ void load_tile_vec(const IdT* src, int64_t* dst, int lane);
-
-template <>
-__device__ __forceinline__ void load_tile_vec<int64_t>(const int64_t* src, int64_t* dst, int lane) {
-    // 64 ids = 512 bytes = one 16-byte load per lane
-    const longlong2 v = __ldg(reinterpret_cast<const longlong2*>(src) + lane);
-    reinterpret_cast<longlong2*>(dst)[lane] = v;
-}
-
-template <>
-__device__ __forceinline__ void load_tile_vec<int32_t>(const int32_t* src, int64_t* dst, int lane) {
-    // 64 ids = 256 bytes = one 16-byte load for each of 16 lanes
-    if (lane < 16) {
-        const int4 v = __ldg(reinterpret_cast<const int4*>(src) + lane);
-        longlong2* d = reinterpret_cast<longlong2*>(dst) + 2 * lane;
-        d[0] = make_longlong2((long long)v.x, (long long)v.y);
-        d[1] = make_longlong2((long long)v.z, (long long)v.w);
-    }
-}
-
 // Per-block shared-memory layout, in order (all offsets 16-byte aligned):
 //   head constants of the layer group, structure of arrays:
 //     fast [G*H] uint4, off [G*H] int64 (padded to even), ext [G*H] uint4,
@@ -171,33 +149,122 @@ __device__ __forceinline__ int load_group_constants(const RowIdsParams& p, const
 // attribute this returns at once.
 __device__ __forceinline__ void wait_prior_grid() { cudaGridDependencySynchronize(); }
 
-// Stage a warp tile's ids (and the N-1 ids left of it) in shared memory.
+// A warp tile's ids (and the N-1 ids left of it) staged in shared memory, in
+// two steps so that other loads can be in flight meanwhile: fetch_tile_ids
+// issues the loads into registers (16-byte vectors when the tile is full and
+// aligned: two int64 ids per lane, or four int32 ids on 16 lanes; else at
+// most two per lane), put_tile_ids stores them.
+struct TileIds {
+    int64_t a, b, c, d, halo;
+};
+
+template <typename IdT>
+__device__ __forceinline__ TileIds fetch_tile_ids(const RowIdsParams& p, int64_t t0, int ntile,
+                                                  int N, int lane) {
+    TileIds f = {0, 0, 0, 0, 0};
+    const IdT* ids = static_cast<const IdT*>(p.ids);
+    if (ntile == kTileTokens && p.ids_vec_ok) {
+        if constexpr (sizeof(IdT) == 8) {
+            const longlong2 v = __ldg(reinterpret_cast<const longlong2*>(ids + t0) + lane);
+            f.a = v.x;
+            f.b = v.y;
+        } else if (lane < 16) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(ids + t0) + lane);
+            f.a = v.x;
+            f.b = v.y;
+            f.c = v.z;
+            f.d = v.w;
+        }
+    } else {
+        if (lane < ntile) f.a = load_id<IdT>(ids, t0 + lane);
+        if (lane + 32 < ntile) f.b = load_id<IdT>(ids, t0 + 32 + lane);
+    }
+    if (lane < N - 1 && t0 - 1 - lane >= 0) f.halo = load_id<IdT>(ids, t0 - 1 - lane);
+    return f;
+}
+
+template <typename IdT>
+__device__ __forceinline__ void put_tile_ids(const RowIdsParams& p, const TileIds& f,
+                                             int64_t* ids_s, int64_t t0, int ntile, int N,
+                                             int lane) {
+    if (ntile == kTileTokens && p.ids_vec_ok) {
+        if constexpr (sizeof(IdT) == 8) {
+            reinterpret_cast<longlong2*>(ids_s)[lane] = make_longlong2(f.a, f.b);
+        } else if (lane < 16) {
+            longlong2* d = reinterpret_cast<longlong2*>(ids_s) + 2 * lane;
+            d[0] = make_longlong2(f.a, f.b);
+            d[1] = make_longlong2(f.c, f.d);
+        }
+    } else {
+        if (lane < ntile) ids_s[lane] = f.a;
+        if (lane + 32 < ntile) ids_s[lane + 32] = f.b;
+    }
+    if (lane < N - 1 && t0 - 1 - lane >= 0) ids_s[-1 - lane] = f.halo;
+    __syncwarp();
+}
+
 template <typename IdT>
 __device__ __forceinline__ void stage_ids(const RowIdsParams& p, int64_t* ids_s, int64_t t0,
                                           int ntile, int N, int lane) {
-    const IdT* ids = static_cast<const IdT*>(p.ids);
-    if (ntile == kTileTokens && p.ids_vec_ok) {
-        load_tile_vec<IdT>(ids + t0, ids_s, lane);
-    } else {
-        for (int i = lane; i < ntile; i += 32) ids_s[i] = load_id<IdT>(ids, t0 + i);
+    put_tile_ids<IdT>(p, fetch_tile_ids<IdT>(p, t0, ntile, N, lane), ids_s, t0, ntile, N, lane);
+}
+
+// The request owning token t in the cu_seqlens search mode, found by the
+// whole warp for a warp-uniform t: a 32-way search, one probe per lane per
+// round (two rounds up to 1024 requests).  For well-formed cu_seqlens the
+// lanes whose probe is <= t form a prefix and the owner lies in the last
+// lane's segment; whatever the contents the probes stay in cu[0..B-1] and
+// the range shrinks every round.  Every lane of the warp must call it.
+__device__ __forceinline__ int warp_owner(const RowIdsParams& p, int64_t t, int lane) {
+    int lo = 0, hi = p.B;  // the owner is in [lo, hi)
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int k = lo + lane * step;
+        const bool le = k < hi && (int64_t)__ldg(p.cu + k) <= t;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        lo += (m ? 31 - __clz((int)m) : 0) * step;
+        hi = min(hi, lo + step);
     }
-    if (lane < N - 1 && t0 - 1 - lane >= 0) ids_s[-1 - lane] = load_id<IdT>(ids, t0 - 1 - lane);
-    __syncwarp();
+    return lo;
 }
 
 // The shifted window V(t, 0..N-1) of tile token i with the carried boundary
 // predicate, in two steps so a kernel can issue the index loads early:
-// load_index reads (req, local) and clamps index data outside the
-// addressable ranges; window_at builds V.  The index-free decode is a
-// compile-time choice: a run-time branch here costs the large-prefill
-// kernel about 3% (measured on GB300).
-template <bool kIndexFree>
+// load_index finds (req, local) -- read, synthesised for a decode, or
+// searched in cu_seqlens -- and clamps index data outside the addressable
+// ranges; window_at builds V.  The mode is a compile-time choice: a run-time
+// branch here costs the large-prefill kernel about 3% (measured on GB300).
+template <int kMode>
 __device__ __forceinline__ void load_index(const RowIdsParams& p, int64_t t, bool live,
-                                           int32_t& r_out, int32_t& q_out) {
+                                           int32_t& r_out, int32_t& q_out, int ra = 0,
+                                           int rb = -1) {
     int32_t r = 0, q = 0;
-    if (kIndexFree) {
+    if (kMode == kIdxDecode) {
         // a decode batch without an index: every token is its own request
         r = (int32_t)t;
+    } else if (kMode == kIdxCu) {
+        if (live) {
+            // the request owning t is the last r with cu[r] <= t (an empty
+            // request shares its start with the next one), searched in
+            // [ra, rb] (the whole batch by default; a tiled kernel passes the
+            // owners of its tile's first and last tokens).  The search keeps
+            // cu[lo] <= t < cu[hi] for well-formed cu_seqlens and reads only
+            // cu[ra..rb] whatever the contents.
+            int lo = ra, hi = (rb < 0 ? p.B - 1 : rb) + 1;
+            int32_t start = __ldg(p.cu + lo);
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                const int32_t c = __ldg(p.cu + mid);
+                if ((int64_t)c <= t) {
+                    lo = mid;
+                    start = c;
+                } else {
+                    hi = mid;
+                }
+            }
+            r = lo;
+            q = (int32_t)min(max(t - (int64_t)start, (int64_t)0), t);
+        }
     } else if (live) {
         r = __ldg(p.req + t);
         q = __ldg(p.local + t);
@@ -223,18 +290,18 @@ __device__ __forceinline__ void window_at(const RowIdsParams& p, const int64_t* 
     }
 }
 
-template <typename IdT, int NMAX, int NT, bool kIndexFree>
+template <typename IdT, int NMAX, int NT, int kMode>
 __device__ __forceinline__ void window(const RowIdsParams& p, const int64_t* ids_s, int64_t t0,
                                        int i, bool live, int N, int64_t (&V)[NMAX],
                                        int32_t& r_out, int32_t& q_out) {
-    load_index<kIndexFree>(p, t0 + i, live, r_out, q_out);
+    load_index<kMode>(p, t0 + i, live, r_out, q_out);
     window_at<IdT, NMAX, NT>(p, ids_s, i, live, N, r_out, q_out, V);
 }
 
 // The context carry: the last token of each request writes the request's
 // next ngram_context row, the last N-1 ids of (context row, this batch's
 // tokens) = W(t, N-2), ..., W(t, 0), oldest first.  Without cu_seqlens
-// (index-free decode) every token is the last of its request.
+// (a decode without an index) every token is the last of its request.
 template <typename IdT>
 __device__ __forceinline__ void carry_context(const RowIdsParams& p, const int64_t* ids_s,
                                               int64_t t0, int i, bool live, int N, int32_t r,

@@ -2,9 +2,10 @@
 //
 // Compiled for the PLE configurations this library is tuned for -- (ngram
 // size, heads per order) in {(3,2), (3,4), (4,4), (5,8)}, each with int32 or
-// int64 ids, int64 or int32 row ids, with or without the context carry, with
-// or without an index (the index-free decode) -- every choice at compile
-// time, because a run-time branch in the window costs the large prefill.
+// int64 ids, int64 or int32 row ids, with or without the context carry, and
+// each way of finding a token's request (an index, a decode without one, a
+// search of cu_seqlens) -- every choice at compile time, because a run-time
+// branch in the window costs the large prefill.
 // Each lane hashes two tokens of the 64-token tile (lane and lane + 32) per
 // shared constant load; the fast path stages 32-bit remainders as head pairs
 // in rows of odd pitch (8-byte stores hit 16 distinct bank pairs per half
@@ -117,7 +118,7 @@ __device__ __forceinline__ void split_readout(const uint2* __restrict__ st, OutT
     }
 }
 
-template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, bool kIndexFree>
+template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, int kIdx>
 __global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_fixed_kernel(const RowIdsParams p) {
     static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
@@ -148,12 +149,21 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
     int64_t VA[N], VB[N];
     if (ntile > 0) {
-        // the index loads go out before the ids staging so the two round
-        // trips overlap
+        // the tile's ids are fetched into registers first and stored to
+        // shared memory only after the index is found, so the ids loads and
+        // the index loads (or the cu_seqlens search) are in flight together
+        const TileIds fetched = fetch_tile_ids<IdT>(p, t0, ntile, N, lane);
         int32_t rA, qA, rB, qB;
-        load_index<kIndexFree>(p, t0 + lane, lane < nA, rA, qA);
-        load_index<kIndexFree>(p, t0 + 32 + lane, lane < nB, rB, qB);
-        stage_ids<IdT>(p, ids_s, t0, ntile, N, lane);
+        int ra = 0, rb = -1;
+        if constexpr (kIdx == kIdxCu) {
+            // the requests of the tile's first and last tokens bound every
+            // token's search (a tile inside one request needs none)
+            ra = warp_owner(p, t0, lane);
+            rb = warp_owner(p, t0 + ntile - 1, lane);
+        }
+        load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA, ra, rb);
+        load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB, ra, rb);
+        put_tile_ids<IdT>(p, fetched, ids_s, t0, ntile, N, lane);
         window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
         window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
         if (kCarry && blockIdx.y == 0) {
@@ -253,105 +263,108 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                 __syncwarp();
             }
         }
-        return;
-    }
-
+    } else {
 #pragma unroll 1
-    for (int l = 0; l < gl; ++l) {
-        const int64_t* ml = sm.mul + l * N;
-        const uint4* hf = sm.fast + l * H;
-        uint64_t mixA = (uint64_t)VA[0] * (uint64_t)ml[0];
-        uint64_t mixB = (uint64_t)VB[0] * (uint64_t)ml[0];
+        for (int l = 0; l < gl; ++l) {
+            const int64_t* ml = sm.mul + l * N;
+            const uint4* hf = sm.fast + l * H;
+            uint64_t mixA = (uint64_t)VA[0] * (uint64_t)ml[0];
+            uint64_t mixB = (uint64_t)VB[0] * (uint64_t)ml[0];
 #pragma unroll
-        for (int s = 1; s < N; ++s) {
-            const uint64_t m = (uint64_t)ml[s];
-            mixA ^= (uint64_t)VA[s] * m;
-            mixB ^= (uint64_t)VB[s] * m;
-            const OffsetBinary uA = offset_binary(mixA);
-            const OffsetBinary uB = offset_binary(mixB);
+            for (int s = 1; s < N; ++s) {
+                const uint64_t m = (uint64_t)ml[s];
+                mixA ^= (uint64_t)VA[s] * m;
+                mixB ^= (uint64_t)VB[s] * m;
+                const OffsetBinary uA = offset_binary(mixA);
+                const OffsetBinary uB = offset_binary(mixB);
 #pragma unroll
-            for (int j = 0; j < HPT; j += 2) {
-                const int h = (s - 1) * HPT + j;
-                const uint4 c0 = hf[h];
-                const uint4 c1 = hf[h + 1];
-                const uint32_t n0 = c0.z << 1, n1 = c1.z << 1;  // -2v of each head
-                stAw[lane * P2 + h / 2] =
-                    make_uint2(floormod_fast(uA, c0, n0), floormod_fast(uA, c1, n1));
-                stAw[(32 + lane) * P2 + h / 2] =
-                    make_uint2(floormod_fast(uB, c0, n0), floormod_fast(uB, c1, n1));
+                for (int j = 0; j < HPT; j += 2) {
+                    const int h = (s - 1) * HPT + j;
+                    const uint4 c0 = hf[h];
+                    const uint4 c1 = hf[h + 1];
+                    const uint32_t n0 = c0.z << 1, n1 = c1.z << 1;  // -2v of each head
+                    stAw[lane * P2 + h / 2] =
+                        make_uint2(floormod_fast(uA, c0, n0), floormod_fast(uA, c1, n1));
+                    stAw[(32 + lane) * P2 + h / 2] =
+                        make_uint2(floormod_fast(uB, c0, n0), floormod_fast(uB, c1, n1));
+                }
             }
-        }
-        __syncwarp();
-        OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
-        if constexpr (U == 1) {
-            // this lane's readout columns' offsets for layer l
-            longlong2 offs[NU];
+            __syncwarp();
+            OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
+            if constexpr (U == 1) {
+                // this lane's readout columns' offsets for layer l
+                longlong2 offs[NU];
 #pragma unroll
-            for (int k = 0; k < NU; ++k) {
-                int col = r0 + k * GU;
-                col = col >= KU ? col - KU : col;
-                offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
-            }
-            long long* d = reinterpret_cast<long long*>(dst);
-            if (full && vec_out) {
-                readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
-                readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
-                                                         soff, stok, offs);
-            } else if (vec_out) {
-                readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
-                if (nB > 0)
-                    readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                              nB, soff, stok, offs);
+                for (int k = 0; k < NU; ++k) {
+                    int col = r0 + k * GU;
+                    col = col >= KU ? col - KU : col;
+                    offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
+                }
+                long long* d = reinterpret_cast<long long*>(dst);
+                if (full && vec_out) {
+                    readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                    readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                             soff, stok, offs);
+                } else if (vec_out) {
+                    readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                    if (nB > 0)
+                        readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                                  nB, soff, stok, offs);
+                } else {
+                    readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                    if (nB > 0)
+                        readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                                   nB, soff, stok, offs);
+                }
             } else {
-                readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
-                if (nB > 0)
-                    readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                               nB, soff, stok, offs);
-            }
-        } else {
-            int4 offs[NU];
+                int4 offs[NU];
 #pragma unroll
-            for (int k = 0; k < NU; ++k) {
-                int col = r0 + k * GU;
-                col = col >= KU ? col - KU : col;
-                offs[k] = *reinterpret_cast<const int4*>(sm.off32 + l * H + 4 * col);
+                for (int k = 0; k < NU; ++k) {
+                    int col = r0 + k * GU;
+                    col = col >= KU ? col - KU : col;
+                    offs[k] = *reinterpret_cast<const int4*>(sm.off32 + l * H + 4 * col);
+                }
+                int* d = reinterpret_cast<int*>(dst);
+                if (full && vec_out) {
+                    readout_quads<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                    readout_quads<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                             soff, stok, offs);
+                } else if (vec_out) {
+                    readout_quads<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                    if (nB > 0)
+                        readout_quads<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                                  nB, soff, stok, offs);
+                } else {
+                    readout_quads<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                    if (nB > 0)
+                        readout_quads<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                                   nB, soff, stok, offs);
+                }
             }
-            int* d = reinterpret_cast<int*>(dst);
-            if (full && vec_out) {
-                readout_quads<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
-                readout_quads<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
-                                                         soff, stok, offs);
-            } else if (vec_out) {
-                readout_quads<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
-                if (nB > 0)
-                    readout_quads<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                              nB, soff, stok, offs);
-            } else {
-                readout_quads<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
-                if (nB > 0)
-                    readout_quads<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                               nB, soff, stok, offs);
-            }
+            __syncwarp();
         }
-        __syncwarp();
     }
 }
 
-template <typename IdT, typename OutT, bool kCarry, bool kIndexFree>
+template <typename IdT, typename OutT, bool kCarry, int kIdx>
 KernelFn pick_fixed(int N, int hpn) {
-    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT, kCarry, kIndexFree>;
-    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT, kCarry, kIndexFree>;
-    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT, kCarry, kIndexFree>;
-    return row_ids_fixed_kernel<IdT, 5, 8, OutT, kCarry, kIndexFree>;
+    if (N == 3 && hpn == 2) return row_ids_fixed_kernel<IdT, 3, 2, OutT, kCarry, kIdx>;
+    if (N == 3 && hpn == 4) return row_ids_fixed_kernel<IdT, 3, 4, OutT, kCarry, kIdx>;
+    if (N == 4 && hpn == 4) return row_ids_fixed_kernel<IdT, 4, 4, OutT, kCarry, kIdx>;
+    return row_ids_fixed_kernel<IdT, 5, 8, OutT, kCarry, kIdx>;
+}
+
+template <typename IdT, typename OutT, bool kCarry>
+KernelFn pick_fixed(int N, int hpn, int mode) {
+    if (mode == kIdxDecode) return pick_fixed<IdT, OutT, kCarry, kIdxDecode>(N, hpn);
+    if (mode == kIdxCu) return pick_fixed<IdT, OutT, kCarry, kIdxCu>(N, hpn);
+    return pick_fixed<IdT, OutT, kCarry, kIdxArrays>(N, hpn);
 }
 
 template <typename IdT, typename OutT>
-KernelFn pick_fixed(int N, int hpn, bool carry, bool index_free) {
-    if (index_free)
-        return carry ? pick_fixed<IdT, OutT, true, true>(N, hpn)
-                     : pick_fixed<IdT, OutT, false, true>(N, hpn);
-    return carry ? pick_fixed<IdT, OutT, true, false>(N, hpn)
-                 : pick_fixed<IdT, OutT, false, false>(N, hpn);
+KernelFn pick_fixed(int N, int hpn, bool carry, int mode) {
+    return carry ? pick_fixed<IdT, OutT, true>(N, hpn, mode)
+                 : pick_fixed<IdT, OutT, false>(N, hpn, mode);
 }
 
 }  // namespace
@@ -359,14 +372,14 @@ KernelFn pick_fixed(int N, int hpn, bool carry, bool index_free) {
 cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                  cudaStream_t stream) {
     const bool carry = p.next_ctx != nullptr;
-    const bool free = p.index_free != 0;
+    const int mode = p.index_mode;
     KernelFn fn;
     if (p.out_bytes == 4)
-        fn = id_bytes == 4 ? pick_fixed<int32_t, int32_t>(p.N, p.hpn, carry, free)
-                           : pick_fixed<int64_t, int32_t>(p.N, p.hpn, carry, free);
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int32_t>(p.N, p.hpn, carry, mode)
+                           : pick_fixed<int64_t, int32_t>(p.N, p.hpn, carry, mode);
     else
-        fn = id_bytes == 4 ? pick_fixed<int32_t, int64_t>(p.N, p.hpn, carry, free)
-                           : pick_fixed<int64_t, int64_t>(p.N, p.hpn, carry, free);
+        fn = id_bytes == 4 ? pick_fixed<int32_t, int64_t>(p.N, p.hpn, carry, mode)
+                           : pick_fixed<int64_t, int64_t>(p.N, p.hpn, carry, mode);
     return launch_fn(fn, p, cfg, stream);
 }
 

@@ -51,10 +51,14 @@ row_ids_kernel(const RowIdsParams p) {
         if (nsub <= 0) break;
         int64_t V[NMAX];
         int32_t r, q;
-        if (p.index_free)
-            window<IdT, NMAX, NT, true>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r, q);
+        if (p.index_mode == kIdxDecode)
+            window<IdT, NMAX, NT, kIdxDecode>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r,
+                                              q);
+        else if (p.index_mode == kIdxCu)
+            window<IdT, NMAX, NT, kIdxCu>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r, q);
         else
-            window<IdT, NMAX, NT, false>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r, q);
+            window<IdT, NMAX, NT, kIdxArrays>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r,
+                                              q);
         if (carry) carry_context<IdT>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, r, q);
 #pragma unroll 1
         for (int l = 0; l < gl; ++l) {

@@ -26,9 +26,9 @@
 namespace ple {
 namespace {
 
-// kIndexFree and kPrepared are compile-time: as run-time branches, the index
+// kIdx and kPrepared are compile-time: as run-time branches, the index
 // choice alone added about 0.15 us to a decode call (measured on GB300).
-template <typename IdT, int NT, bool kIndexFree, bool kPrepared>
+template <typename IdT, int NT, int kIdx, bool kPrepared>
 __global__ void __launch_bounds__(kSmallMaxThreads)
 row_ids_small_kernel(const RowIdsParams p) {
     constexpr int NMAX = NT > 0 ? NT : PLE_MAX_NGRAM;
@@ -47,7 +47,7 @@ row_ids_small_kernel(const RowIdsParams p) {
     const int64_t off = kPrepared ? 0 : __ldg(reinterpret_cast<const long long*>(p.offsets) + k);
 
     int32_t r, q;
-    load_index<kIndexFree>(p, t, true, r, q);
+    load_index<kIdx>(p, t, true, r, q);
     const IdT* ids = static_cast<const IdT*>(p.ids);
     const IdT* crow = static_cast<const IdT*>(p.ctx) + (int64_t)r * (N - 1) + (N - 1) + q;
     const long long* ml = reinterpret_cast<const long long*>(p.mult) + (int64_t)l * N;
@@ -91,22 +91,27 @@ row_ids_small_kernel(const RowIdsParams p) {
     }
 }
 
-template <typename IdT, bool kIndexFree, bool kPrepared>
+template <typename IdT, int kIdx, bool kPrepared>
 KernelFn pick_small(int N) {
     switch (N) {
-        case 3: return row_ids_small_kernel<IdT, 3, kIndexFree, kPrepared>;
-        case 4: return row_ids_small_kernel<IdT, 4, kIndexFree, kPrepared>;
-        case 5: return row_ids_small_kernel<IdT, 5, kIndexFree, kPrepared>;
-        default: return row_ids_small_kernel<IdT, 0, kIndexFree, kPrepared>;
+        case 3: return row_ids_small_kernel<IdT, 3, kIdx, kPrepared>;
+        case 4: return row_ids_small_kernel<IdT, 4, kIdx, kPrepared>;
+        case 5: return row_ids_small_kernel<IdT, 5, kIdx, kPrepared>;
+        default: return row_ids_small_kernel<IdT, 0, kIdx, kPrepared>;
     }
+}
+
+template <typename IdT, int kIdx>
+KernelFn pick_small(const RowIdsParams& p) {
+    return p.heads != nullptr ? pick_small<IdT, kIdx, true>(p.N)
+                              : pick_small<IdT, kIdx, false>(p.N);
 }
 
 template <typename IdT>
 KernelFn pick_small(const RowIdsParams& p) {
-    const bool prepared = p.heads != nullptr;
-    if (p.index_free)
-        return prepared ? pick_small<IdT, true, true>(p.N) : pick_small<IdT, true, false>(p.N);
-    return prepared ? pick_small<IdT, false, true>(p.N) : pick_small<IdT, false, false>(p.N);
+    if (p.index_mode == kIdxDecode) return pick_small<IdT, kIdxDecode>(p);
+    if (p.index_mode == kIdxCu) return pick_small<IdT, kIdxCu>(p);
+    return pick_small<IdT, kIdxArrays>(p);
 }
 
 }  // namespace

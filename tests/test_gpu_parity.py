@@ -671,6 +671,136 @@ def test_prepared_heads_replace_vocab_and_offsets(kernel):
     assert_same(out, oracle_rows(batch), "prepared heads, no vocab / offsets")
 
 
+def batch_cu(batch):
+    """The batch's cu_seqlens (a decode's is 0, 1, ..., B)."""
+    if batch.cu_seqlens is not None:
+        return batch.cu_seqlens
+    return np.arange(batch.num_requests + 1, dtype=np.int32)
+
+
+def gpu_rows_search(batch, out_dtype=torch.int64, carry=False, prepared=False, out=None):
+    """Row ids with req = local = None and cu_seqlens: the kernel searches
+    cu_seqlens for each token's request (no index built or read)."""
+    ctx = dev(batch.ngram_context)
+    nxt = torch.full_like(ctx, -5) if carry else None
+    heads = (ple.ple_prepare_heads(dev(batch.vocab_sizes), dev(batch.offsets))
+             if prepared else None)
+    got = ple.ple_row_ids(dev(batch.ids), None, None, ctx, dev(batch.layer_multipliers),
+                          dev(batch.vocab_sizes), dev(batch.offsets), batch.ngram_size,
+                          batch.heads_per_ngram, batch.boundary_id, out=out, out_dtype=out_dtype,
+                          cu_seqlens=dev(batch_cu(batch)), next_context=nxt, heads=heads)
+    return got, nxt
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_cu_search_mode_full_size(name):
+    """Every workload with the index found in the kernel from cu_seqlens:
+    the same rows (int64 and int32, derived and prepared constants) and the
+    same carried context as the oracle."""
+    batch = WORKLOADS[name]
+    exp = oracle_rows(batch)
+    out, nxt = gpu_rows_search(batch, carry=True)
+    assert_same(out, exp, f"{name} search mode")
+    assert_same(nxt, oracle_carry(batch), f"{name} search mode carry")
+    out, _ = gpu_rows_search(batch, out_dtype=torch.int32, prepared=True)
+    assert_same(out, low32(exp), f"{name} search mode, int32, prepared")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("chunk", range(3))
+def test_cu_search_mode_random_edges(chunk, kernel):
+    """Empty requests (repeated cu_seqlens entries, at the start, the end and
+    in runs), one-token requests, decodes given as cu_seqlens, ragged tiles,
+    with the carry and int32 row ids in turn."""
+    for seed in range(chunk * 50, (chunk + 1) * 50):
+        batch = for_kernel(wl.random_batch(17000 + seed, T_max=150,
+                                           ids_dtype=np.int32 if seed % 2 else np.int64), kernel)
+        out_dtype = torch.int32 if seed % 3 == 0 else torch.int64
+        out, nxt = gpu_rows_search(batch, out_dtype=out_dtype, carry=seed % 4 == 1,
+                                   prepared=seed % 5 == 2)
+        exp = oracle_rows(batch)
+        assert_same(out, low32(exp) if out_dtype == torch.int32 else exp, f"search {seed}")
+        if nxt is not None:
+            assert_same(nxt, oracle_carry(batch), f"search carry {seed}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_cu_search_mode_many_requests(kernel):
+    """Thousands of requests, many of them empty or one token long, so the
+    search runs a dozen steps and tiles span many requests."""
+    rng = np.random.default_rng(4321)
+    B = 3000 if kernel == "tiled" else 1000
+    lengths = rng.choice([0, 1, 1, 2, 5, 40], size=B)
+    T = int(lengths.sum())
+    base = wl.random_batch(99, N=4, hpn=4, L=1, T_max=10, decode_batch=False)
+    batch = dataclasses.replace(
+        base, ids=rng.integers(0, wl.VOCAB, size=T, dtype=np.int64),
+        ngram_context=rng.integers(0, wl.VOCAB, size=(B, 3), dtype=np.int64),
+        cu_seqlens=wl.cu_from_lengths(lengths))
+    batch = for_kernel(batch, kernel)
+    out, nxt = gpu_rows_search(batch, carry=True)
+    assert_same(out, oracle_rows(batch), "many requests")
+    assert_same(nxt, oracle_carry(batch), "many requests carry")
+
+
+def test_cu_search_mode_in_a_graph():
+    """A prefill step of one launch (no index build) captured once and
+    replayed with fresh ids and contexts."""
+    b0 = wl.ragged_16()
+    ids, ctx = dev(b0.ids), dev(b0.ngram_context)
+    M, vocab, off = dev(b0.layer_multipliers), dev(b0.vocab_sizes), dev(b0.offsets)
+    cu = dev(b0.cu_seqlens)
+    out = torch.full((1, b0.num_tokens, b0.num_heads), -1, dtype=torch.int64, device=DEV)
+
+    def step():
+        ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, b0.ngram_size, b0.heads_per_ngram,
+                        b0.boundary_id, out=out, cu_seqlens=cu)
+
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    torch.cuda.synchronize(DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for replay in (1, 2, 3):
+        rng = np.random.default_rng(600 + replay)
+        fresh_ids = wl.uniform_ids(rng, b0.num_tokens, 0.02)
+        fresh_ctx = wl.uniform_ids(rng, b0.num_requests * 2, 0.02).reshape(-1, 2)
+        nb = dataclasses.replace(b0, ids=fresh_ids, ngram_context=fresh_ctx)
+        ids.copy_(dev(nb.ids))
+        ctx.copy_(dev(nb.ngram_context))
+        g.replay()
+        torch.cuda.synchronize(DEV)
+        assert_same(out, oracle_rows(nb), f"search-mode replay {replay}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_cu_search_mode_malformed_cu_stays_in_bounds(kernel):
+    """cu_seqlens is device data the host cannot check.  Malformed contents
+    (negative, past T, decreasing) give unspecified rows but no access
+    outside the arrays: the canaries around the output and the carried
+    context survive, and the call completes."""
+    batch = for_kernel(wl.random_batch(5150, N=4, hpn=2, L=1, T_max=100, decode_batch=False),
+                       kernel)
+    L, T, H, B = batch.num_layers, batch.num_tokens, batch.num_heads, batch.num_requests
+    rng = np.random.default_rng(3)
+    cu = rng.choice([-(2 ** 31), -5, 0, 3, T, T + 7, 2 ** 31 - 1], size=B + 1).astype(np.int32)
+    buf = torch.full((L * T * H + 2,), 0x5A5A, dtype=torch.int64, device=DEV)
+    out = buf[1:-1].view(L, T, H)
+    ctx = dev(batch.ngram_context)
+    nbuf = torch.full((B * 3 + 2,), 77, dtype=torch.int64, device=DEV)
+    nxt = nbuf[1:-1].view(B, 3)
+    ple.ple_row_ids(dev(batch.ids), None, None, ctx, dev(batch.layer_multipliers),
+                    dev(batch.vocab_sizes), dev(batch.offsets), 4, 2, batch.boundary_id, out=out,
+                    cu_seqlens=dev(cu), next_context=nxt)
+    torch.cuda.synchronize(DEV)
+    assert int(buf[0]) == 0x5A5A and int(buf[-1]) == 0x5A5A
+    assert int(nbuf[0]) == 77 and int(nbuf[-1]) == 77
+
+
 @pytest.mark.parametrize("extra", [0, 1])
 def test_small_and_tiled_kernels_meet_at_the_threshold(extra):
     """The large prefill's first tokens, as many as the small-batch kernel

@@ -126,6 +126,11 @@ def row_ids_ex(lib, **kw):
     # call gets past the pointer checks to the output dtype
     (dict(vocab=None, off=None, heads=A, out_dtype=2), ple.PLE_ERR_DTYPE),
     (dict(vocab=None, off=None, heads=A, ids=None), ple.PLE_ERR_NULL),
+    # req = local = NULL with cu_seqlens: the kernel searches cu_seqlens, so
+    # B != T is accepted (the call gets past the index checks to out_dtype)
+    (dict(req=None, local=None, T=4, B=5, out_dtype=2), ple.PLE_ERR_DTYPE),
+    (dict(req=None, local=None, T=4, B=5, cu=A + 2), ple.PLE_ERR_ALIGN),
+    (dict(cu=A + 2, nxt=None), ple.PLE_ERR_ALIGN),
 ])
 def test_row_ids_ex_host_checks(lib, kw, status):
     assert row_ids_ex(lib, **kw) == status
