@@ -209,23 +209,72 @@ __device__ __forceinline__ void stage_ids(const RowIdsParams& p, int64_t* ids_s,
     put_tile_ids<IdT>(p, fetch_tile_ids<IdT>(p, t0, ntile, N, lane), ids_s, t0, ntile, N, lane);
 }
 
-// The request owning token t in the cu_seqlens search mode, found by the
-// whole warp for a warp-uniform t: a 32-way search, one probe per lane per
-// round (two rounds up to 1024 requests).  For well-formed cu_seqlens the
-// lanes whose probe is <= t form a prefix and the owner lies in the last
-// lane's segment; whatever the contents the probes stay in cu[0..B-1] and
-// the range shrinks every round.  Every lane of the warp must call it.
-__device__ __forceinline__ int warp_owner(const RowIdsParams& p, int64_t t, int lane) {
-    int lo = 0, hi = p.B;  // the owner is in [lo, hi)
-    while (hi - lo > 1) {
-        const int step = (hi - lo + 31) >> 5;
-        const int k = lo + lane * step;
-        const bool le = k < hi && (int64_t)__ldg(p.cu + k) <= t;
-        const unsigned m = __ballot_sync(0xffffffffu, le);
-        lo += (m ? 31 - __clz((int)m) : 0) * step;
-        hi = min(hi, lo + step);
+// The requests owning tokens t1 and t2 in the cu_seqlens search mode, found
+// by the whole warp for warp-uniform t1, t2: a 32-way search, one probe per
+// lane per round for each (two rounds up to 1024 requests), the two in
+// lockstep.  For well-formed cu_seqlens the lanes whose probe is <= t form
+// a prefix and the owner lies in the last such lane's segment; whatever the
+// contents the probes stay in cu[0..B-1] and each range shrinks every round.
+// Every lane of the warp must call it.
+__device__ __forceinline__ void warp_owners(const RowIdsParams& p, int64_t t1, int64_t t2,
+                                            int lane, int& r1, int& r2) {
+    int lo1 = 0, hi1 = p.B, lo2 = 0, hi2 = p.B;  // the owners are in [lo, hi)
+    while (hi1 - lo1 > 1 || hi2 - lo2 > 1) {
+        const int step1 = (hi1 - lo1 + 31) >> 5;
+        const int step2 = (hi2 - lo2 + 31) >> 5;
+        const int k1 = lo1 + lane * step1;
+        const int k2 = lo2 + lane * step2;
+        const bool le1 = hi1 - lo1 > 1 && k1 < hi1 && (int64_t)__ldg(p.cu + k1) <= t1;
+        const bool le2 = hi2 - lo2 > 1 && k2 < hi2 && (int64_t)__ldg(p.cu + k2) <= t2;
+        const unsigned m1 = __ballot_sync(0xffffffffu, le1);
+        const unsigned m2 = __ballot_sync(0xffffffffu, le2);
+        if (hi1 - lo1 > 1) {
+            lo1 += (m1 ? 31 - __clz((int)m1) : 0) * step1;
+            hi1 = min(hi1, lo1 + step1);
+        }
+        if (hi2 - lo2 > 1) {
+            lo2 += (m2 ? 31 - __clz((int)m2) : 0) * step2;
+            hi2 = min(hi2, lo2 + step2);
+        }
     }
-    return lo;
+    r1 = lo1;
+    r2 = lo2;
+}
+
+// The owners of a lane's two tokens tA, tB of a tile whose requests are
+// ra..rb with rb - ra <= 32: lane j holds the start cu[ra + 1 + j] of one of
+// the tile's later requests (past rb: a sentinel above every token), and a
+// token's owner is ra plus the number of those starts at or below it -- for
+// well-formed cu_seqlens a prefix of the lanes, counted by a 5-step shuffle
+// search with no memory round trip.  Whatever the contents, only cu[ra..rb]
+// is read and the results are clamped as load_index clamps them.  Every lane
+// of the warp must call it.
+__device__ __forceinline__ void tile_owners(const RowIdsParams& p, int ra, int rb, int64_t tA,
+                                            bool liveA, int64_t tB, bool liveB, int lane,
+                                            int32_t& rA, int32_t& qA, int32_t& rB,
+                                            int32_t& qB) {
+    const int k = ra + 1 + lane;
+    const int32_t s = k <= rb ? __ldg(p.cu + k) : INT32_MAX;
+    const int32_t s0 = __ldg(p.cu + ra);
+    int cA = 0, cB = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) {
+        const int32_t vA = __shfl_sync(0xffffffffu, s, cA + step - 1);
+        const int32_t vB = __shfl_sync(0xffffffffu, s, cB + step - 1);
+        if ((int64_t)vA <= tA) cA += step;
+        if ((int64_t)vB <= tB) cB += step;
+    }
+    const int32_t last = __shfl_sync(0xffffffffu, s, 31);
+    if (cA == 31 && (int64_t)last <= tA) cA = 32;
+    if (cB == 31 && (int64_t)last <= tB) cB = 32;
+    const int32_t pA = __shfl_sync(0xffffffffu, s, max(cA - 1, 0));
+    const int32_t pB = __shfl_sync(0xffffffffu, s, max(cB - 1, 0));
+    const int64_t startA = cA ? pA : s0;
+    const int64_t startB = cB ? pB : s0;
+    rA = liveA ? min(max(ra + cA, 0), p.B - 1) : 0;
+    rB = liveB ? min(max(ra + cB, 0), p.B - 1) : 0;
+    qA = liveA ? (int32_t)min(max(tA - startA, (int64_t)0), tA) : 0;
+    qB = liveB ? (int32_t)min(max(tB - startB, (int64_t)0), tB) : 0;
 }
 
 // The shifted window V(t, 0..N-1) of tile token i with the carried boundary

@@ -154,15 +154,33 @@ row_ids_fixed_kernel(const RowIdsParams p) {
         // the index loads (or the cu_seqlens search) are in flight together
         const TileIds fetched = fetch_tile_ids<IdT>(p, t0, ntile, N, lane);
         int32_t rA, qA, rB, qB;
-        int ra = 0, rb = -1;
         if constexpr (kIdx == kIdxCu) {
             // the requests of the tile's first and last tokens bound every
-            // token's search (a tile inside one request needs none)
-            ra = warp_owner(p, t0, lane);
-            rb = warp_owner(p, t0 + ntile - 1, lane);
+            // token's owner: with at most 32 requests between them the lanes
+            // rank the requests' starts (no search at all inside one
+            // request), else each lane searches between them
+            int ra, rb;
+            warp_owners(p, t0, t0 + ntile - 1, lane, ra, rb);
+            if (ra == rb) {
+                // the whole tile inside one request
+                const int64_t start = __ldg(p.cu + ra);
+                rA = lane < nA ? ra : 0;
+                rB = lane < nB ? ra : 0;
+                qA = lane < nA ? (int32_t)min(max(t0 + lane - start, (int64_t)0), t0 + lane) : 0;
+                qB = lane < nB
+                         ? (int32_t)min(max(t0 + 32 + lane - start, (int64_t)0), t0 + 32 + lane)
+                         : 0;
+            } else if (rb - ra <= 32) {
+                tile_owners(p, ra, rb, t0 + lane, lane < nA, t0 + 32 + lane, lane < nB, lane, rA,
+                            qA, rB, qB);
+            } else {
+                load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA, ra, rb);
+                load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB, ra, rb);
+            }
+        } else {
+            load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA);
+            load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB);
         }
-        load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA, ra, rb);
-        load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB, ra, rb);
         put_tile_ids<IdT>(p, fetched, ids_s, t0, ntile, N, lane);
         window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
         window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
