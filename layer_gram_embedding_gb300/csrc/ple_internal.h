@@ -27,6 +27,12 @@ constexpr int kFixedMinBlocks = PLE_FIXED_MIN_BLOCKS;
 #define PLE_BLOCKS_PER_SM 16
 #endif
 constexpr int kTargetBlocksPerSm = PLE_BLOCKS_PER_SM;
+// A grid with fewer blocks than this many per SM (times the SM count) takes
+// fewer warps per block, so that its warps spread over more SMs (0: never).
+#ifndef PLE_SPREAD_BLOCKS_PER_SM
+#define PLE_SPREAD_BLOCKS_PER_SM 1
+#endif
+constexpr int kSpreadBlocksPerSm = PLE_SPREAD_BLOCKS_PER_SM;
 // Shared-memory budget for the per-head constants of one layer group.
 constexpr int kConstBudgetBytes = 48 * 1024;
 // Batches of at most this many row ids (T * H * L) take the small-batch

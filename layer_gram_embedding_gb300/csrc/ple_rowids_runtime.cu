@@ -131,6 +131,11 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
 
     const size_t fixed = head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
     while (warps > 1 && fixed + warps * per_warp > (size_t)dev.max_smem_optin) --warps;
+    // a small grid (a medium batch with few layers) spreads its warp tiles
+    // over more SMs with fewer warps per block
+    while (warps > 1 && ((tiles + warps - 1) / warps) * groups <
+                            (int64_t)kSpreadBlocksPerSm * dev.sm_count)
+        --warps;
     blocks_x = (tiles + warps - 1) / warps;
     cfg.grid = dim3((unsigned)blocks_x, (unsigned)groups, 1);
     cfg.block = dim3(32 * warps, 1, 1);
