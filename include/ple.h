@@ -261,16 +261,22 @@ ple_status ple_prepare_heads(const int64_t* vocab_sizes, const int64_t* offsets,
  * accumulated in fp32 in head order (h = 0 first); a row id outside
  * [0, table_rows) adds nothing.  One launch for every layer.
  *
- *   all arguments up to boundary_id: as ple_row_ids (req = local = NULL is
- *                 the index-free decode).
+ *   all arguments up to boundary_id: as ple_row_ids_ex (req = local = NULL:
+ *                 the requests found from cu_seqlens when it is given, else
+ *                 a decode batch).
  *   table         [L, table_rows, dim] bfloat16 (as raw 16-bit patterns),
  *                 device, 16-byte aligned; may be NULL when table_rows == 0.
  *   table_rows    V >= 0 rows per layer.
  *   dim           D, a multiple of 8 in [8, PLE_MAX_EMBED_DIM].
  *   out           [L, T, D] float, device, 16-byte aligned; every element is
  *                 written.
+ *   cu_seqlens    optional [B+1] int32, device: with req = local = NULL, the
+ *                 layout the kernel searches for each token's request (as in
+ *                 ple_row_ids_ex); not read when req and local are given.
+ *   heads         optional: constants from ple_prepare_heads, as in
+ *                 ple_row_ids_ex (vocab_sizes and offsets may then be NULL).
  *
- * Errors: as ple_row_ids, plus PLE_ERR_SIZE for dim / table_rows and
+ * Errors: as ple_row_ids_ex, plus PLE_ERR_SIZE for dim / table_rows and
  * PLE_ERR_ALIGN for a table or out that is not 16-byte aligned.
  */
 ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_tokens,
@@ -279,7 +285,8 @@ ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_to
                          const int64_t* vocab_sizes, const int64_t* offsets, int32_t num_heads,
                          int32_t ngram_size, int32_t heads_per_ngram, int32_t num_layers,
                          int64_t boundary_id, const void* table, int64_t table_rows, int32_t dim,
-                         float* out, void* stream);
+                         float* out, const int32_t* cu_seqlens, const void* heads,
+                         void* stream);
 
 /*
  * ple_validate_index -- diagnostic: check the index preconditions on the

@@ -49,7 +49,7 @@ SIGNATURES = {
                               _I32, _I32, _I64, _P, _I32, _P, _P, _P, _P]),
     "ple_prepare_heads": (_I32, [_P, _P, _I32, _I32, _P, _P]),
     "ple_row_embed": (_I32, [_P, _I32, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, _I32, _I32,
-                             _I32, _I32, _I64, _P, _I64, _I32, _P, _P]),
+                             _I32, _I32, _I64, _P, _I64, _I32, _P, _P, _P, _P]),
     "ple_validate_index": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P, _P]),
     "ple_selftest_floor_mod": (_I32, [_P, _P, _I64, _P, _P, _P]),
     "ple_status_string": (ctypes.c_char_p, [_I32]),
@@ -312,16 +312,21 @@ def ple_row_embed(input_ids: torch.Tensor, req: torch.Tensor | None, local: torc
                   ngram_context: torch.Tensor, layer_multipliers: torch.Tensor,
                   vocab_sizes: torch.Tensor, offsets: torch.Tensor, ngram_size: int,
                   heads_per_ngram: int, boundary_id: int, table: torch.Tensor,
-                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                  out: torch.Tensor | None = None, stream=None,
+                  cu_seqlens: torch.Tensor | None = None,
+                  heads: torch.Tensor | None = None) -> torch.Tensor:
     """[L, T, D] float32: per layer and token, the sum over heads of the rows
     of `table` ([L, V, D] bfloat16, or its raw 16-bit patterns) that the row
     ids name -- the hash and the gather in one launch, the row ids never
-    written.  Other arguments as ple_row_ids."""
+    written.  Other arguments as ple_row_ids (req = local = None with
+    cu_seqlens: the requests found in the kernel; heads: prepared
+    constants)."""
     where = "ple_row_embed"
     if (req is None) != (local is None):
         raise ValueError(f"{where}: pass both req and local, or neither (decode)")
     dev = _one_cuda_device([t for t in (input_ids, req, local, ngram_context, layer_multipliers,
-                                        vocab_sizes, offsets, table, out) if t is not None], where)
+                                        vocab_sizes, offsets, table, out, cu_seqlens, heads)
+                            if t is not None], where)
     if table.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
         raise TypeError(f"{where}: table must be bfloat16 (or its 16-bit patterns)")
     if table.dim() != 3 or not table.is_contiguous():
@@ -348,6 +353,16 @@ def ple_row_embed(input_ids: torch.Tensor, req: torch.Tensor | None, local: torc
         if tuple(out.shape) != (L, T, D):
             raise ValueError(f"{where}: out must be [L, T, D]")
     ctx = ngram_context
+    use_cu = cu_seqlens is not None and req is None
+    if use_cu:
+        _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+        if cu_seqlens.numel() != ctx.shape[0] + 1:
+            raise ValueError(f"{where}: cu_seqlens must be [B + 1]")
+    if heads is not None:
+        _need(heads, torch.uint8, "heads", where)
+        if tuple(heads.shape) != (L, H, PLE_HEAD_BYTES):
+            raise ValueError(f"{where}: heads must be ple_prepare_heads' [L, H, "
+                             f"{PLE_HEAD_BYTES}]")
     with torch.cuda.device(dev):
         st = lib().ple_row_embed(
             _ptr(input_ids), PLE_I64 if input_ids.dtype == torch.int64 else PLE_I32, T,
@@ -355,6 +370,8 @@ def ple_row_embed(input_ids: torch.Tensor, req: torch.Tensor | None, local: torc
             _ptr(local) if local is not None else ctypes.c_void_p(0), _ptr(ctx), ctx.shape[0],
             ctx.shape[1], _ptr(M), _ptr(vocab), _ptr(off), H, int(ngram_size),
             int(heads_per_ngram), L, int(boundary_id), _ptr(table), V, D, _ptr(out),
+            _ptr(cu_seqlens) if use_cu else ctypes.c_void_p(0),
+            _ptr(heads) if heads is not None else ctypes.c_void_p(0),
             _stream_handle(stream, dev))
     _check(st, where)
     return out

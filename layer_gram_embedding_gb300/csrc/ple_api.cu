@@ -252,13 +252,14 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
                                     int32_t num_heads, int32_t ngram_size,
                                     int32_t heads_per_ngram, int32_t num_layers,
                                     int64_t boundary_id, const void* table, int64_t table_rows,
-                                    int32_t dim, float* out, void* stream) {
+                                    int32_t dim, float* out, const int32_t* cu_seqlens,
+                                    const void* heads, void* stream) {
     ple::RowIdsParams p;
     bool empty = false;
     ple_status st = check_row_args(input_ids, id_dtype, num_tokens, req, local, ngram_context,
                                    num_requests, ctx_len, layer_multipliers, vocab_sizes, offsets,
                                    num_heads, ngram_size, heads_per_ngram, num_layers, boundary_id,
-                                   nullptr, nullptr, &p, &empty);
+                                   cu_seqlens, heads, &p, &empty);
     if (st != PLE_OK) return st;
     if (dim < 8 || dim % 8 != 0 || dim > PLE_MAX_EMBED_DIM || table_rows < 0) return PLE_ERR_SIZE;
     // the table's byte size must fit in 64 bits

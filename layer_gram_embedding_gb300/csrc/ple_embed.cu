@@ -13,9 +13,9 @@
 // The work is an HBM gather: each (token, layer) reads H rows of 2*D bytes at
 // random and writes 4*D bytes.  Each lane owns one 16-byte slice (8 values)
 // of a row, so a warp reads a 512-byte row (D = 256) in one instruction;
-// four heads' slices are loaded before they are accumulated, so every lane
-// keeps four independent 16-byte loads in flight.  Narrower rows put several
-// tokens in one warp pass; wider rows loop over slices.
+// eight heads' slices are loaded before they are accumulated, so every lane
+// keeps up to eight independent 16-byte loads in flight.  Narrower rows put
+// several tokens in one warp pass; wider rows loop over slices.
 #include "ple_rowids_common.cuh"
 
 namespace ple {
@@ -42,21 +42,28 @@ __device__ __forceinline__ uint4 load_slice(const uint4* __restrict__ tab, int64
     return __ldg(tab + row * slices + c);
 }
 
-// Sum the table rows named by one token's H staged row ids, for slice c.
+// Sum the table rows named by one token's H staged row ids, for slice c:
+// eight heads' loads are issued before any of them is accumulated (then
+// four, then one at a time), so a lane keeps up to eight 16-byte loads in
+// flight; the sum stays in head order.
 __device__ __forceinline__ void gather_token(const int64_t* __restrict__ rows, int H,
                                              const uint4* __restrict__ tab, int64_t V,
                                              int slices, int c, float* __restrict__ dst) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     int h = 0;
+    for (; h + 8 <= H; h += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = load_slice(tab, rows[h + k], V, slices, c);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) accumulate8(acc, v[k]);
+    }
     for (; h + 4 <= H; h += 4) {
-        const uint4 a = load_slice(tab, rows[h], V, slices, c);
-        const uint4 b = load_slice(tab, rows[h + 1], V, slices, c);
-        const uint4 d = load_slice(tab, rows[h + 2], V, slices, c);
-        const uint4 e = load_slice(tab, rows[h + 3], V, slices, c);
-        accumulate8(acc, a);
-        accumulate8(acc, b);
-        accumulate8(acc, d);
-        accumulate8(acc, e);
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = load_slice(tab, rows[h + k], V, slices, c);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) accumulate8(acc, v[k]);
     }
     for (; h < H; ++h) accumulate8(acc, load_slice(tab, rows[h], V, slices, c));
     float4* o = reinterpret_cast<float4*>(dst + 8 * c);
@@ -64,8 +71,16 @@ __device__ __forceinline__ void gather_token(const int64_t* __restrict__ rows, i
     __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
 }
 
-template <typename IdT, int NT>
-__global__ void __launch_bounds__(kMaxWarps * 32)
+// The gather's rate depends on how many table loads are in flight, which
+// the register budget decides: eight loads a lane under a budget of seven
+// resident blocks a SM (72 registers) measured best on GB300 (large prefill,
+// D = 256: 1.93 ms a call, against 1.97 at eight blocks, 2.03 at six, and
+// 2.12 for four loads a lane with the compiler's own budget).  The index
+// mode is compile-time, as in the row-id kernels.
+constexpr int kEmbedMinBlocks = 7;
+
+template <typename IdT, int NT, int kIdx>
+__global__ void __launch_bounds__(kMaxWarps * 32, kEmbedMinBlocks)
 row_embed_kernel(const RowIdsParams p, const EmbedArgs e) {
     constexpr int NMAX = NT > 0 ? NT : PLE_MAX_NGRAM;
     const int N = NT > 0 ? NT : p.N;
@@ -106,14 +121,7 @@ row_embed_kernel(const RowIdsParams p, const EmbedArgs e) {
         if (nsub <= 0) break;
         int64_t V[NMAX];
         int32_t r, q;
-        if (p.index_mode == kIdxDecode)
-            window<IdT, NMAX, NT, kIdxDecode>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r,
-                                              q);
-        else if (p.index_mode == kIdxCu)
-            window<IdT, NMAX, NT, kIdxCu>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r, q);
-        else
-            window<IdT, NMAX, NT, kIdxArrays>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r,
-                                              q);
+        window<IdT, NMAX, NT, kIdx>(p, ids_s, t0, 32 * u + lane, lane < nsub, N, V, r, q);
 #pragma unroll 1
         for (int l = 0; l < gl; ++l) {
             const int hb = l * H;
@@ -141,27 +149,31 @@ row_embed_kernel(const RowIdsParams p, const EmbedArgs e) {
     }
 }
 
+using EmbedFn = void (*)(const RowIdsParams, const EmbedArgs);
+
+template <typename IdT, int kIdx>
+EmbedFn pick_embed(int N) {
+    switch (N) {
+        case 3: return row_embed_kernel<IdT, 3, kIdx>;
+        case 4: return row_embed_kernel<IdT, 4, kIdx>;
+        case 5: return row_embed_kernel<IdT, 5, kIdx>;
+        default: return row_embed_kernel<IdT, 0, kIdx>;
+    }
+}
+
+template <typename IdT>
+EmbedFn pick_embed(int N, int mode) {
+    if (mode == kIdxDecode) return pick_embed<IdT, kIdxDecode>(N);
+    if (mode == kIdxCu) return pick_embed<IdT, kIdxCu>(N);
+    return pick_embed<IdT, kIdxArrays>(N);
+}
+
 }  // namespace
 
 cudaError_t launch_row_embed(const RowIdsParams& p, const EmbedArgs& e, int id_bytes,
                              const RowIdsLaunch& cfg, cudaStream_t stream) {
-    using EmbedFn = void (*)(const RowIdsParams, const EmbedArgs);
-    EmbedFn fn;
-    if (id_bytes == 4) {
-        switch (p.N) {
-            case 3: fn = row_embed_kernel<int32_t, 3>; break;
-            case 4: fn = row_embed_kernel<int32_t, 4>; break;
-            case 5: fn = row_embed_kernel<int32_t, 5>; break;
-            default: fn = row_embed_kernel<int32_t, 0>; break;
-        }
-    } else {
-        switch (p.N) {
-            case 3: fn = row_embed_kernel<int64_t, 3>; break;
-            case 4: fn = row_embed_kernel<int64_t, 4>; break;
-            case 5: fn = row_embed_kernel<int64_t, 5>; break;
-            default: fn = row_embed_kernel<int64_t, 0>; break;
-        }
-    }
+    const EmbedFn fn = id_bytes == 4 ? pick_embed<int32_t>(p.N, p.index_mode)
+                                     : pick_embed<int64_t>(p.N, p.index_mode);
     if (cfg.smem_bytes > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)cfg.smem_bytes);

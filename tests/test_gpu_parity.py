@@ -300,18 +300,25 @@ def test_chunked_prefill_through_the_carry_equals_one_prefill():
     assert_same(got, whole, "chunked prefill through the carry")
 
 
-def check_embed(batch, table, index_free=False, what=""):
+def check_embed(batch, table, index_free=False, what="", search=False, prepared=False):
     """GPU gather vs the oracle's exact (double) sum: fp32 recursive summation
-    of H terms errs by at most (H-1) * 2^-24 * sum|x| per element."""
+    of H terms errs by at most (H-1) * 2^-24 * sum|x| per element.  search:
+    no index, the requests found from cu_seqlens in the kernel; prepared:
+    head constants from ple_prepare_heads."""
     t = torch.from_numpy(table.view(np.int16)).to(DEV)
-    if index_free:
+    cu = None
+    if index_free or search:
         req = local = None
+        cu = dev(batch_cu(batch)) if search else None
     else:
         req, local = gpu_index(batch)
+    heads = (ple.ple_prepare_heads(dev(batch.vocab_sizes), dev(batch.offsets))
+             if prepared else None)
     got = ple.ple_row_embed(dev(batch.ids), req, local, dev(batch.ngram_context),
                             dev(batch.layer_multipliers), dev(batch.vocab_sizes),
                             dev(batch.offsets), batch.ngram_size, batch.heads_per_ngram,
-                            batch.boundary_id, t).cpu().numpy().astype(np.float64)
+                            batch.boundary_id, t, cu_seqlens=cu,
+                            heads=heads).cpu().numpy().astype(np.float64)
     oreq, olocal = oracle_index(batch)
     exact, abs_sum = oracle.row_embed(batch.ids, oreq, olocal, batch.ngram_context,
                                       batch.layer_multipliers, batch.vocab_sizes, batch.offsets,
@@ -328,7 +335,10 @@ def test_row_embed_random_batches(D):
     for seed in range(12):
         batch, table = wl.small_table_batch(12000 + 31 * D + seed, D=D, T_max=150,
                                             ids_dtype=np.int32 if seed % 2 else np.int64)
-        check_embed(batch, table, what=f"D={D} seed={seed}")
+        # every third batch finds its requests from cu_seqlens in the kernel,
+        # every fourth uses prepared head constants
+        check_embed(batch, table, what=f"D={D} seed={seed}", search=seed % 3 == 1,
+                    prepared=seed % 4 == 2)
 
 
 def test_row_embed_rows_outside_the_table_add_nothing():

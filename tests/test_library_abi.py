@@ -152,11 +152,12 @@ def test_prepare_heads_host_checks(lib, args, status):
 
 def row_embed(lib, **kw):
     a = dict(ids=A, dtype=1, T=64, req=A, local=A, ctx=A, B=1, ctx_len=2, M=A, vocab=A, off=A,
-             H=4, N=3, hpn=2, L=1, b=7, table=A, V=100, D=64, out=A)
+             H=4, N=3, hpn=2, L=1, b=7, table=A, V=100, D=64, out=A, cu=None, heads=None)
     a.update(kw)
     return lib.ple_row_embed(a["ids"], a["dtype"], a["T"], a["req"], a["local"], a["ctx"],
                              a["B"], a["ctx_len"], a["M"], a["vocab"], a["off"], a["H"], a["N"],
-                             a["hpn"], a["L"], a["b"], a["table"], a["V"], a["D"], a["out"], None)
+                             a["hpn"], a["L"], a["b"], a["table"], a["V"], a["D"], a["out"],
+                             a["cu"], a["heads"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -171,6 +172,12 @@ def row_embed(lib, **kw):
     (dict(table=A + 8), ple.PLE_ERR_ALIGN),
     (dict(out=A + 4), ple.PLE_ERR_ALIGN),
     (dict(T=0, table=None, out=None), ple.PLE_OK),
+    (dict(heads=A + 8), ple.PLE_ERR_ALIGN),
+    (dict(req=None, local=None, T=4, B=5, cu=A + 2), ple.PLE_ERR_ALIGN),
+    # with cu_seqlens B != T is accepted: the call gets past the index checks
+    (dict(req=None, local=None, T=4, B=5, cu=A, table=A + 8), ple.PLE_ERR_ALIGN),
+    (dict(req=None, local=None, T=4, B=5), ple.PLE_ERR_SIZE),          # decode needs B == T
+    (dict(vocab=None, off=None, heads=A, D=12), ple.PLE_ERR_SIZE),     # past the NULL checks
 ])
 def test_row_embed_host_checks(lib, kw, status):
     assert row_embed(lib, **kw) == status
