@@ -141,8 +141,9 @@ row_ids_fixed_kernel(const RowIdsParams p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTileTokens;
-    const int ntile = (int)max((int64_t)0, min((int64_t)kTileTokens, p.T - t0));
+    constexpr int kTile = fixed_tile_tokens(H, kIdx);  // 64, or 32 (see there)
+    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTile;
+    const int ntile = (int)max((int64_t)0, min((int64_t)kTile, p.T - t0));
     int64_t* ids_s = sm.ids + warp * (kHaloSlots + kTileTokens) + kHaloSlots;
     unsigned char* stage = sm.stage + (size_t)warp * stage_bytes(H, true);
     const int nA = min(32, ntile);
@@ -183,10 +184,16 @@ row_ids_fixed_kernel(const RowIdsParams p) {
         }
         put_tile_ids<IdT>(p, fetched, ids_s, t0, ntile, N, lane);
         window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
-        window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
+        if constexpr (kTile == 64) {
+            window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
+        } else {
+#pragma unroll
+            for (int s = 0; s < N; ++s) VB[s] = 0;
+        }
         if (kCarry && blockIdx.y == 0) {
             carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
-            carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
+            if constexpr (kTile == 64)
+                carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
         }
     }
     const bool all_fast = __syncthreads_and(fast_vote) != 0;

@@ -108,9 +108,10 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     if (!runtime_layout && small_batch_fits(p)) return plan_small(p);
     RowIdsLaunch cfg;
     cfg.small = false;
-    const int64_t tiles = (p.T + kTileTokens - 1) / kTileTokens;
-    int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
     const bool fixed_shape = !runtime_layout && uses_fixed_kernel(p);
+    const int tile = fixed_shape ? fixed_tile_tokens(p.H, p.index_mode) : kTileTokens;
+    const int64_t tiles = (p.T + tile - 1) / tile;
+    int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
     p.stage_pitch = p.H | 1;
     const size_t per_warp =
         (size_t)(kHaloSlots + kTileTokens) * 8 + stage_bytes(p.H, fixed_shape);
