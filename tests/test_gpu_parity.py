@@ -384,14 +384,21 @@ def test_random_edge_batches(chunk, kernel):
 def test_fixed_shapes_random_edges(N, hpn, kernel):
     """The tuned shapes with ragged tiles, empty requests, boundary densities
     0..1 and every kind of vocab size (so both the 32-bit fast path and the
-    general path, whose staging the 32-head shape splits), int64 row ids."""
+    general path, whose staging the 32-head shape splits), int64 row ids,
+    reading an index and finding the requests from cu_seqlens."""
     for seed in range(30):
         dtype = np.int32 if seed % 2 else np.int64
         batch = for_kernel(wl.random_batch(15000 + 100 * N + 10 * hpn + seed, N=N, hpn=hpn,
                                            T_max=200, ids_dtype=dtype,
                                            vocab_mode="primes" if seed % 3 == 0 else "mixed"),
                            kernel)
-        assert_same(gpu_rows(batch), oracle_rows(batch), f"N={N} hpn={hpn} seed {seed}")
+        exp = oracle_rows(batch)
+        assert_same(gpu_rows(batch), exp, f"N={N} hpn={hpn} seed {seed}")
+        # the same batch with the requests found from cu_seqlens in the kernel
+        # (the 32-head shape then takes 32-token tiles), with the carry
+        out, nxt = gpu_rows_search(batch, carry=True, prepared=seed % 4 == 3)
+        assert_same(out, exp, f"N={N} hpn={hpn} seed {seed} search mode")
+        assert_same(nxt, oracle_carry(batch), f"N={N} hpn={hpn} seed {seed} search carry")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
