@@ -24,7 +24,9 @@
  *     is written.  A launch failure is reported as PLE_ERR_CUDA; the CUDA
  *     error code is then available from ple_last_cuda_error().
  *   - Pointers must be aligned to their element size (4 bytes for int32
- *     arrays, 8 for int64 arrays); 16-byte alignment is not required.
+ *     arrays, 8 for int64 arrays); 16-byte alignment is not required except
+ *     where an entry point says so (prepared head constants, the gather's
+ *     table and output).
  *   - All integer arithmetic is int64 with two's-complement wrap-around, as
  *     torch's int64 tensor ops do.
  */
@@ -140,7 +142,8 @@ ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests
  * in that order, before anything else), then PLE_ERR_NULL (one of req /
  * local NULL, or any other pointer), PLE_ERR_SIZE (both NULL with B != T),
  * PLE_ERR_DTYPE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
- * One kernel launch; no host reads; fixed grid for fixed (T, L, H, N).
+ * One kernel launch; no host reads; the grid depends only on the sizes, the
+ * way the index is given and the device (so a captured graph replays it).
  * Batches of at most ple_small_batch_max_rows() row ids (T * H * L) run the
  * small-batch kernel, one thread per row id; larger ones the tiled kernels.
  * The row ids are the same either way.
