@@ -43,8 +43,8 @@ enum : uint32_t {
 
 // One head's constants, kept structure-of-arrays in shared memory so the
 // fast path reads 16 bytes per head and the offset separately:
-//   fast  = {m_lo, m_hi, -|v| mod 2^32, D low word}, m = floor((2^64-1)/|v|),
-//           D = |v| - (2^63 mod |v|)
+//   fast  = {m_lo, m_hi, -2|v| mod 2^32 (fast heads), D low word},
+//           m = floor((2^64-1)/|v|), D = |v| - (2^63 mod |v|)
 //   off   = the head's row offset
 //   ext   = {|v| high word, D high word, kHead* flags, |v| low word}
 struct HeadConst {
@@ -70,7 +70,7 @@ __host__ __device__ __forceinline__ HeadConst make_head_const(int64_t v, int64_t
     if (v < 0) kind |= kHeadNegative;
     if (va == 0) kind |= kHeadZero;
     if (v > 0 && va <= (1ull << 29)) kind |= kHeadFast;
-    c.fast = make_uint4((uint32_t)m, (uint32_t)(m >> 32), 0u - (uint32_t)va, (uint32_t)d);
+    c.fast = make_uint4((uint32_t)m, (uint32_t)(m >> 32), 0u - 2u * (uint32_t)va, (uint32_t)d);
     c.off = off;
     c.ext = make_uint4((uint32_t)(va >> 32), (uint32_t)(d >> 32), kind, (uint32_t)va);
     return c;
@@ -110,27 +110,32 @@ __device__ __forceinline__ OffsetBinary offset_binary(uint64_t mix) {
 }
 
 // floormod(x, v) for 0 < v <= 2^29 from x's offset binary u, given
-// c = {m_lo, m_hi, -v, D} and nv2 = -2v (mod 2^32).  The quotient estimate
+// c = {m_lo, m_hi, -2v, D} and nv = -v (mod 2^32; the caller derives it
+// once per head by an arithmetic shift of -2v).  With -2v, the constant the
+// first two corrections add, in the loaded word rather than computed, those
+// adds no longer go to the integer-multiply pipe (measured on GB300: 1.4
+// fewer multiply-pipe instructions per row id, the ALU count unchanged, so
+// they fuse into the min).  The quotient estimate
 // keeps only the three partial products that reach bits 64..95 of u*m and
 // drops the carry out of bits 32..63 (at most 2), so it can fall 3 short of
 // floor(u/v): the remainder estimate lies in [0, 4v), plus D in [1, 5v) <
 // 2^32, and three conditional subtractions (2v, 2v, v) finish it.  The
 // partial products are summed inside the multiplies (mul.hi, mad.hi,
 // mad.lo) and each correction is min(r + (-k), r) on unsigned values.
-__device__ __forceinline__ uint32_t floormod_fast(OffsetBinary u, uint4 c, uint32_t nv2) {
+__device__ __forceinline__ uint32_t floormod_fast(OffsetBinary u, uint4 c, uint32_t nv) {
     uint32_t t1, t2, q, r;
     asm("mul.hi.u32 %0, %1, %2;" : "=r"(t1) : "r"(u.lo), "r"(c.y));
     asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(t2) : "r"(u.hi), "r"(c.x), "r"(t1));
     asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(q) : "r"(u.hi), "r"(c.y), "r"(t2));
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(c.z), "r"(u.lo + c.w));
-    r = min(r + nv2, r);  // in [1, 5v): subtract 2v if it stays non-negative
-    r = min(r + nv2, r);
-    r = min(r + c.z, r);  // and v
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(nv), "r"(u.lo + c.w));
+    r = min(r + c.z, r);  // in [1, 5v): subtract 2v if it stays non-negative
+    r = min(r + c.z, r);
+    r = min(r + nv, r);  // and v
     return r;
 }
 
 __device__ __forceinline__ int64_t row_fast(OffsetBinary u, uint4 c, int64_t off) {
-    return (int64_t)((uint64_t)off + floormod_fast(u, c, c.z << 1));
+    return (int64_t)((uint64_t)off + floormod_fast(u, c, (uint32_t)((int32_t)c.z >> 1)));
 }
 
 // floormod(x, v) + off for any head.

@@ -278,8 +278,9 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                         const int h = (s - 1) * HPT + j;
                         const uint4 c0 = hf[h];
                         const uint4 c1 = hf[h + 1];
-                        stAw[lane * P2 + h / 2] = make_uint2(floormod_fast(uu, c0, c0.z << 1),
-                                                             floormod_fast(uu, c1, c1.z << 1));
+                        stAw[lane * P2 + h / 2] = make_uint2(
+                            floormod_fast(uu, c0, (uint32_t)((int32_t)c0.z >> 1)),
+                            floormod_fast(uu, c1, (uint32_t)((int32_t)c1.z >> 1)));
                     }
                 }
                 __syncwarp();
@@ -307,7 +308,8 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                     const int h = (s - 1) * HPT + j;
                     const uint4 c0 = hf[h];
                     const uint4 c1 = hf[h + 1];
-                    const uint32_t n0 = c0.z << 1, n1 = c1.z << 1;  // -2v of each head
+                    const uint32_t n0 = (uint32_t)((int32_t)c0.z >> 1);  // -v of each head
+                    const uint32_t n1 = (uint32_t)((int32_t)c1.z >> 1);
                     stAw[lane * P2 + h / 2] =
                         make_uint2(floormod_fast(uA, c0, n0), floormod_fast(uA, c1, n1));
                     stAw[(32 + lane) * P2 + h / 2] =
