@@ -57,11 +57,21 @@ KERNEL_SOURCES = ["ple_rowids_common.cuh", "ple_rowids_fixed.cu", "ple_divmod.cu
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "row_ids_prefill_262144_traffic.json")
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines: a comment edit leaves
+    the kernel, and so its recorded traffic, unchanged."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "layer_gram_embedding_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "layer_gram_embedding_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

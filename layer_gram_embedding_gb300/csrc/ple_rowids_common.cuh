@@ -1,6 +1,7 @@
 // The PLE n-gram row-id hash on sm_103a: device code shared by the fixed-shape
-// kernel (ple_rowids_fixed.cu) and the runtime-shape kernel
-// (ple_rowids_runtime.cu).
+// kernel (ple_rowids_fixed.cu), the runtime-shape kernel
+// (ple_rowids_runtime.cu), the small-batch kernel (ple_rowids_small.cu) and
+// the fused table gather (ple_embed.cu).
 //
 // Computes, for every token of a ragged batch and every layer, head and
 // n-gram order, the table row id of FreeToken PR #338 ("perf(ple): fuse the
@@ -20,10 +21,13 @@
 //   - grid.x covers the tokens in warp tiles of 64; grid.y splits the layers
 //     into groups so that even a small T fills the SMs.
 //   - Block prologue: the group's per-head divisor constants (one reciprocal
-//     per head, see ple_divmod.cuh) and multipliers go to shared memory.
-//   - Each warp stages its tile's ids plus an ngram_size-1 halo in shared
-//     memory (16-byte vector loads when aligned) and builds each token's
-//     window V in registers with the carried boundary predicate.
+//     per head, see ple_divmod.cuh, or loaded when prepared once) and
+//     multipliers go to shared memory.
+//   - Each warp finds its tokens' (request, offset) -- read from an index,
+//     synthesised for a decode, or searched in cu_seqlens -- while its tile's
+//     ids plus an ngram_size-1 halo load (16-byte vectors when aligned), then
+//     stages the ids in shared memory and builds each token's window V in
+//     registers with the carried boundary predicate.
 //   - Fixed shapes (the tuned (ngram_size, heads_per_ngram) pairs, even
 //     heads per order): each lane hashes two tokens per shared constant load,
 //     stages 32-bit remainders as head pairs in rows of odd pitch (8-byte

@@ -11,8 +11,11 @@
 // in rows of odd pitch (8-byte stores hit 16 distinct bank pairs per half
 // warp), and the readout walks the tile in global order ([L, T, H]), adds
 // each head's offset in registers and stores 16 bytes per lane, so a warp
-// store covers 512 consecutive bytes.  Heads off the 32-bit fast path (vocab
-// outside (0, 2^29]) stage int64 rows and read them out 8 bytes at a time.
+// store covers 512 consecutive bytes.  Shapes with more than 16 heads stage
+// one 32-token half (a 16-token quarter on the general path) at a time, and
+// in the cu_seqlens search mode take 32-token tiles.  Heads off the 32-bit
+// fast path (vocab outside (0, 2^29]) stage int64 rows and read them out 8
+// bytes at a time.
 #include "ple_rowids_common.cuh"
 
 namespace ple {
