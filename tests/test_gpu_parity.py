@@ -864,3 +864,31 @@ def test_stream_argument_is_honoured():
         out = gpu_rows(batch)
     s.synchronize()
     assert_same(out, oracle_rows(batch), "side stream")
+
+
+def test_binding_refuses_malformed_new_arguments():
+    """The binding's checks on the prepared constants and cu_seqlens: wrong
+    shape, dtype or length is a ValueError / TypeError before any launch."""
+    b = wl.prefill_512()
+    ids, ctx = dev(b.ids), dev(b.ngram_context)
+    M, vocab, off = dev(b.layer_multipliers), dev(b.vocab_sizes), dev(b.offsets)
+    heads = ple.ple_prepare_heads(vocab, off)
+    assert tuple(heads.shape) == (1, 4, ple.PLE_HEAD_BYTES) and heads.dtype == torch.uint8
+    args = (ids, None, None, ctx, M, vocab, off, 3, 2, b.boundary_id)
+    with pytest.raises(ValueError):
+        ple.ple_row_ids(*args, heads=heads[:, :3])  # wrong number of heads
+    with pytest.raises(TypeError):
+        ple.ple_row_ids(*args, heads=heads.view(torch.int8))  # not uint8
+    with pytest.raises(ValueError):
+        ple.ple_row_ids(*args, cu_seqlens=dev(np.array([0, 256, 512], np.int32)))  # B + 1 != 2
+    with pytest.raises(TypeError):
+        ple.ple_row_ids(*args, cu_seqlens=dev(np.array([0, 512], np.int64)))  # not int32
+    with pytest.raises(ValueError):
+        ple.ple_prepare_heads(vocab, off[:, :3])  # shapes differ
+    with pytest.raises(ValueError):
+        req, _ = gpu_index(b)
+        ple.ple_row_ids(ids, req, None, ctx, M, vocab, off, 3, 2, b.boundary_id)  # one of two
+    # and the well-formed calls agree
+    exp = oracle_rows(b)
+    assert_same(ple.ple_row_ids(*args, heads=heads, cu_seqlens=dev(b.cu_seqlens)), exp,
+                "well-formed search mode with prepared constants")
