@@ -95,14 +95,14 @@ constexpr int kSplitStageHeads = 16;
 
 __host__ __device__ constexpr int fast_stage_rows(int H) { return H > kSplitStageHeads ? 32 : 64; }
 // Tokens per warp tile of the fixed-shape kernel.  A split-staging shape
-// hashes one 32-token half at a time anyway, so in the cu_seqlens search
-// mode it takes 32-token tiles: a tile then spans at most 32 requests and
-// always takes the lane ranking, never the per-lane search (a 64-token tile
-// of one-token requests spans 64).  Measured on GB300 for the 48-layer mixed
-// batch: 19.0 -> 18.3 us in the search mode; with an index the 64-token tile
-// stays faster (18.0 against 18.3: half as many block prologues).
-__host__ __device__ constexpr int fixed_tile_tokens(int H, int mode) {
-    return H > kSplitStageHeads && mode == kIdxCu ? 32 : kTileTokens;
+// hashes one 32-token half at a time anyway, so it takes 32-token tiles:
+// twice the warp tiles for grids that are short of them (the 48-layer mixed
+// batch has 128 tiles of 64), and in the cu_seqlens search mode a tile spans
+// at most 32 requests, so it always takes the lane ranking.  Measured on
+// GB300 for the mixed batch, with int64 row ids at 32 blocks per SM: 18.0 ->
+// 16.6 us reading an index, 18.3 -> 17.3 us in the search mode.
+__host__ __device__ constexpr int fixed_tile_tokens(int H) {
+    return H > kSplitStageHeads ? 32 : kTileTokens;
 }
 __host__ __device__ constexpr int general_stage_rows(int H) {
     return H > kSplitStageHeads ? 16 : 32;

@@ -156,7 +156,7 @@ row_ids_fixed_kernel(const RowIdsParams p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr int kTile = fixed_tile_tokens(H, kIdx);  // 64, or 32 (see there)
+    constexpr int kTile = fixed_tile_tokens(H);  // 64, or 32 (see there)
     const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kTile;
     const int ntile = (int)max((int64_t)0, min((int64_t)kTile, p.T - t0));
     int64_t* ids_s = sm.ids + warp * (kHaloSlots + kTileTokens) + kHaloSlots;

@@ -109,7 +109,7 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     RowIdsLaunch cfg;
     cfg.small = false;
     const bool fixed_shape = !runtime_layout && uses_fixed_kernel(p);
-    const int tile = fixed_shape ? fixed_tile_tokens(p.H, p.index_mode) : kTileTokens;
+    const int tile = fixed_shape ? fixed_tile_tokens(p.H) : kTileTokens;
     const int64_t tiles = (p.T + tile - 1) / tile;
     int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
     p.stage_pitch = p.H | 1;
