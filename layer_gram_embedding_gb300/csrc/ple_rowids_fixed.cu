@@ -9,13 +9,14 @@
 // Each lane hashes two tokens of the 64-token tile (lane and lane + 32) per
 // shared constant load; the fast path stages 32-bit remainders as head pairs
 // in rows of odd pitch (8-byte stores hit 16 distinct bank pairs per half
-// warp), and the readout walks the tile in global order ([L, T, H]), adds
-// each head's offset in registers and stores 16 bytes per lane, so a warp
-// store covers 512 consecutive bytes.  Shapes with more than 16 heads stage
-// one 32-token half (a 16-token quarter on the general path) at a time, and
-// in the cu_seqlens search mode take 32-token tiles.  Heads off the 32-bit
-// fast path (vocab outside (0, 2^29]) stage int64 rows and read them out 8
-// bytes at a time.
+// warp) -- or, for int32 row ids, as swizzled head quads (16-byte stores and
+// loads without bank conflicts) -- and the readout walks the tile in global
+// order ([L, T, H]), adds each head's offset in registers and stores 16 bytes
+// per lane, so a warp store covers 512 consecutive bytes.  Shapes with more
+// than 16 heads stage one 32-token half (a 16-token quarter on the general
+// path) at a time, and in the cu_seqlens search mode take 32-token tiles.
+// Heads off the 32-bit fast path (vocab outside (0, 2^29]) stage int64 rows
+// and read them out 8 bytes at a time.
 #include "ple_rowids_common.cuh"
 
 namespace ple {
@@ -52,9 +53,12 @@ __device__ __forceinline__ void readout_pairs(const uint2* __restrict__ st,
     }
 }
 
-// int32 row ids: four heads (two staged pairs) per 16-byte lane store; the
-// offsets' low words are added in 32-bit arithmetic (the low 32 bits of the
-// int64 row id).  K2 quads per token.
+// int32 row ids of the split staging (more than 16 heads, pair staging):
+// four heads (two staged pairs) per 16-byte lane store; the offsets' low
+// words are added in 32-bit arithmetic (the low 32 bits of the int64 row
+// id).  K2 quads per token.  At 32 heads the pitch of 17 pairs puts the two
+// tokens a half warp reads in opposite bank parities, so the pair loads are
+// conflict-free.
 template <int K2, int P2, int NC, int GSTEP, bool kVec, bool kFull>
 __device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int* __restrict__ dst,
                                               int lane, int nsub, const int (&soff)[K2],
@@ -68,6 +72,52 @@ __device__ __forceinline__ void readout_quads(const uint2* __restrict__ st, int*
             const int4 o = offs[((32 * j) % K2) / GSTEP];
             const int4 rows = make_int4((int)((unsigned)o.x + a.x), (int)((unsigned)o.y + a.y),
                                         (int)((unsigned)o.z + b.x), (int)((unsigned)o.w + b.y));
+            if (kVec) {
+                __stcs(d4 + 32 * j + lane, rows);
+            } else {
+                int* d1 = reinterpret_cast<int*>(d4 + 32 * j + lane);
+                __stcs(d1, rows.x);
+                __stcs(d1 + 1, rows.y);
+                __stcs(d1 + 2, rows.z);
+                __stcs(d1 + 3, rows.w);
+            }
+        }
+    }
+}
+
+// Quad staging of int32 remainders (shapes of at most 16 heads): four heads
+// per 16-byte slot, K2 = H / 4 slots per token, no padding, slot index
+// token * K2 + (quad ^ quad_swizzle(token)).  A 16-byte shared access is
+// served eight lanes at a time, conflict-free when the eight slots differ
+// modulo 8: for odd K2 consecutive tokens already do, both when a lane
+// stores its own token's quads and when the readout's lanes walk the tile
+// in global order; for K2 a power of two the quad index is XORed with the
+// token's rank among the 8 / K2 tokens one readout phase covers.  The
+// swizzle repeats every 32 tokens, so the tile's second half uses the same.
+template <int K2>
+__device__ __forceinline__ int quad_swizzle(int token) {
+    static_assert(K2 % 2 == 1 || K2 == 2 || K2 == 4 || K2 == 8, "quad staging layout");
+    if constexpr (K2 % 2 == 1)
+        return 0;
+    else
+        return (token / (8 / K2)) % K2;
+}
+
+// int32 row ids from quad staging: one 16-byte shared load per 16-byte
+// global store (K2 per lane per half tile).
+template <int K2, int NC, int GSTEP, bool kVec, bool kFull>
+__device__ __forceinline__ void readout_quad_slots(const uint4* __restrict__ st,
+                                                   int* __restrict__ dst, int lane, int nsub,
+                                                   const int (&soff)[K2], const int (&stok)[K2],
+                                                   const int4 (&offs)[NC]) {
+    int4* d4 = reinterpret_cast<int4*>(dst);
+#pragma unroll
+    for (int j = 0; j < K2; ++j) {
+        if (kFull || stok[j] < nsub) {
+            const uint4 a = st[soff[j]];
+            const int4 o = offs[((32 * j) % K2) / GSTEP];
+            const int4 rows = make_int4((int)((unsigned)o.x + a.x), (int)((unsigned)o.y + a.y),
+                                        (int)((unsigned)o.z + a.z), (int)((unsigned)o.w + a.w));
             if (kVec) {
                 __stcs(d4 + 32 * j + lane, rows);
             } else {
@@ -121,20 +171,8 @@ __device__ __forceinline__ void split_readout(const uint2* __restrict__ st, OutT
     }
 }
 
-// Register budget: the compiler's own, except for int32 output with at most
-// 16 heads, which is bound by the integer-multiply pipe and gains from nine
-// resident blocks a SM (56 registers): the large prefill's int32 variant
-// 25.2 -> 24.3 us on GB300, while the same budget slows its int64 variant
-// and the 32-head shape (whose split staging needs the registers).
-template <typename IdT, int NT, int HPT, typename OutT>
-constexpr int fixed_min_blocks() {
-    return sizeof(OutT) == 4 && (NT - 1) * HPT <= kSplitStageHeads && kFixedMinBlocks == 0
-               ? 9
-               : kFixedMinBlocks;
-}
-
 template <typename IdT, int NT, int HPT, typename OutT, bool kCarry, int kIdx>
-__global__ void __launch_bounds__(kMaxWarps * 32, (fixed_min_blocks<IdT, NT, HPT, OutT>()))
+__global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_fixed_kernel(const RowIdsParams p) {
     static_assert(NT >= 2 && HPT >= 2 && HPT % 2 == 0, "fixed shapes have even heads_per_ngram");
     constexpr int N = NT;
@@ -260,13 +298,20 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     constexpr int NU = KU / GU;
     const int q0 = lane / KU;
     const int r0 = lane % KU;
+    // int32 row ids of shapes without split staging stage quads (see
+    // quad_swizzle); soff then counts 16-byte slots, else 8-byte pairs
+    constexpr bool kQuadStage = U == 2 && fast_stage_rows(H) == 64;
     int soff[KU], stok[KU];
 #pragma unroll
     for (int j = 0; j < KU; ++j) {
         const int cj = (32 * j) % KU;
         const bool carry = r0 + cj >= KU;
+        const int col = r0 + cj - (carry ? KU : 0);
         stok[j] = q0 + (32 * j) / KU + (carry ? 1 : 0);
-        soff[j] = stok[j] * P2 + U * (r0 + cj - (carry ? KU : 0));
+        if constexpr (kQuadStage)
+            soff[j] = stok[j] * KU + (col ^ quad_swizzle<KU>(stok[j]));
+        else
+            soff[j] = stok[j] * P2 + U * col;
     }
     const bool full = nA == 32 && nB == 32;
     const bool vec_out = p.out_vec_ok != 0;
@@ -304,7 +349,77 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                 __syncwarp();
             }
         }
+    } else if constexpr (kQuadStage) {
+        // int32 row ids: each lane stages its two tokens' remainders four
+        // heads to a 16-byte store, and the readout takes one 16-byte load
+        // per 16-byte global store (with pair staging, the readout's pair
+        // loads met 3-way bank conflicts at 12 heads and made the shared
+        // memory pipe the bound)
+        uint4* stQ = reinterpret_cast<uint4*>(stage);
+        const int sw = quad_swizzle<KU>(lane);  // token 32 + lane's too
+#pragma unroll 1
+        for (int l = 0; l < gl; ++l) {
+            const int64_t* ml = sm.mul + l * N;
+            const uint4* hf = sm.fast + l * H;
+            uint64_t mixA = (uint64_t)VA[0] * (uint64_t)ml[0];
+            uint64_t mixB = (uint64_t)VB[0] * (uint64_t)ml[0];
+            uint32_t rA[H], rB[H];
+#pragma unroll
+            for (int s = 1; s < N; ++s) {
+                const uint64_t m = (uint64_t)ml[s];
+                mixA ^= (uint64_t)VA[s] * m;
+                mixB ^= (uint64_t)VB[s] * m;
+                const OffsetBinary uA = offset_binary(mixA);
+                const OffsetBinary uB = offset_binary(mixB);
+#pragma unroll
+                for (int j = 0; j < HPT; j += 2) {
+                    const int h = (s - 1) * HPT + j;
+                    const uint4 c0 = hf[h];
+                    const uint4 c1 = hf[h + 1];
+                    const uint32_t n0 = (uint32_t)((int32_t)c0.z >> 1);  // -v of each head
+                    const uint32_t n1 = (uint32_t)((int32_t)c1.z >> 1);
+                    rA[h] = floormod_fast(uA, c0, n0);
+                    rA[h + 1] = floormod_fast(uA, c1, n1);
+                    rB[h] = floormod_fast(uB, c0, n0);
+                    rB[h + 1] = floormod_fast(uB, c1, n1);
+                    if (h % 4 == 2) {
+                        // heads h - 2 .. h + 1 complete quad h / 4
+                        const int qd = (h / 4) ^ sw;
+                        stQ[lane * KU + qd] = make_uint4(rA[h - 2], rA[h - 1], rA[h], rA[h + 1]);
+                        stQ[(32 + lane) * KU + qd] =
+                            make_uint4(rB[h - 2], rB[h - 1], rB[h], rB[h + 1]);
+                    }
+                }
+            }
+            __syncwarp();
+            int4 offs[NU];
+#pragma unroll
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                offs[k] = *reinterpret_cast<const int4*>(sm.off32 + l * H + 4 * col);
+            }
+            int* d = reinterpret_cast<int*>(static_cast<OutT*>(p.out) +
+                                            ((int64_t)(l0 + l) * p.T + t0) * H);
+            if (full && vec_out) {
+                readout_quad_slots<KU, NU, GU, true, true>(stQ, d, lane, 32, soff, stok, offs);
+                readout_quad_slots<KU, NU, GU, true, true>(stQ + 32 * KU, d + 32 * H, lane, 32,
+                                                           soff, stok, offs);
+            } else if (vec_out) {
+                readout_quad_slots<KU, NU, GU, true, false>(stQ, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quad_slots<KU, NU, GU, true, false>(stQ + 32 * KU, d + 32 * H, lane,
+                                                                nB, soff, stok, offs);
+            } else {
+                readout_quad_slots<KU, NU, GU, false, false>(stQ, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_quad_slots<KU, NU, GU, false, false>(stQ + 32 * KU, d + 32 * H, lane,
+                                                                 nB, soff, stok, offs);
+            }
+            __syncwarp();
+        }
     } else {
+        // int64 row ids: pair staging, 16-byte readout of one pair per store
 #pragma unroll 1
         for (int l = 0; l < gl; ++l) {
             const int64_t* ml = sm.mul + l * N;
@@ -333,55 +448,29 @@ row_ids_fixed_kernel(const RowIdsParams p) {
             }
             __syncwarp();
             OutT* dst = static_cast<OutT*>(p.out) + ((int64_t)(l0 + l) * p.T + t0) * H;
-            if constexpr (U == 1) {
-                // this lane's readout columns' offsets for layer l
-                longlong2 offs[NU];
+            // this lane's readout columns' offsets for layer l
+            longlong2 offs[NU];
 #pragma unroll
-                for (int k = 0; k < NU; ++k) {
-                    int col = r0 + k * GU;
-                    col = col >= KU ? col - KU : col;
-                    offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
-                }
-                long long* d = reinterpret_cast<long long*>(dst);
-                if (full && vec_out) {
-                    readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
-                    readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
-                                                             soff, stok, offs);
-                } else if (vec_out) {
-                    readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
-                    if (nB > 0)
-                        readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                                  nB, soff, stok, offs);
-                } else {
-                    readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
-                    if (nB > 0)
-                        readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                                   nB, soff, stok, offs);
-                }
+            for (int k = 0; k < NU; ++k) {
+                int col = r0 + k * GU;
+                col = col >= KU ? col - KU : col;
+                offs[k] = *reinterpret_cast<const longlong2*>(sm.off + l * H + 2 * col);
+            }
+            long long* d = reinterpret_cast<long long*>(dst);
+            if (full && vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
+                readout_pairs<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
+                                                         soff, stok, offs);
+            } else if (vec_out) {
+                readout_pairs<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                              nB, soff, stok, offs);
             } else {
-                int4 offs[NU];
-#pragma unroll
-                for (int k = 0; k < NU; ++k) {
-                    int col = r0 + k * GU;
-                    col = col >= KU ? col - KU : col;
-                    offs[k] = *reinterpret_cast<const int4*>(sm.off32 + l * H + 4 * col);
-                }
-                int* d = reinterpret_cast<int*>(dst);
-                if (full && vec_out) {
-                    readout_quads<KU, P2, NU, GU, true, true>(stA, d, lane, 32, soff, stok, offs);
-                    readout_quads<KU, P2, NU, GU, true, true>(stA + 32 * P2, d + 32 * H, lane, 32,
-                                                             soff, stok, offs);
-                } else if (vec_out) {
-                    readout_quads<KU, P2, NU, GU, true, false>(stA, d, lane, nA, soff, stok, offs);
-                    if (nB > 0)
-                        readout_quads<KU, P2, NU, GU, true, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                                  nB, soff, stok, offs);
-                } else {
-                    readout_quads<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
-                    if (nB > 0)
-                        readout_quads<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
-                                                                   nB, soff, stok, offs);
-                }
+                readout_pairs<KU, P2, NU, GU, false, false>(stA, d, lane, nA, soff, stok, offs);
+                if (nB > 0)
+                    readout_pairs<KU, P2, NU, GU, false, false>(stA + 32 * P2, d + 32 * H, lane,
+                                                               nB, soff, stok, offs);
             }
             __syncwarp();
         }
