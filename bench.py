@@ -556,7 +556,14 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
     """The same metric through ple_row_ids (the Python binding; requests
     found from cu_seqlens in the kernel) with host buffers: every step copies
     its ids, cu_seqlens and context from pinned host memory, runs the call,
-    and copies every row id back to pinned host memory."""
+    and copies every row id back to pinned host memory.
+
+    Steps are pipelined over two buffer slots, as a serving loop would run
+    them: step i's device-to-host copy runs on a second stream while step
+    i + 1's host-to-device copy and kernel run on the launching stream; a
+    slot is reused only after its previous copy back has finished.  The
+    timed region ends when the last step's rows are in host memory.  The
+    same steps run one after another on one stream are reported beside it."""
     b0 = batches[0]
     T, B, L, H = b0.num_tokens, b0.num_requests, b0.num_layers, b0.num_heads
     host = []
@@ -564,37 +571,61 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
         host.append(dict(ids=torch.from_numpy(b.ids).pin_memory(),
                          cu=torch.from_numpy(b.cu_seqlens).pin_memory(),
                          ctx=torch.from_numpy(np.ascontiguousarray(b.ngram_context)).pin_memory()))
-    d_ids = torch.empty(T, dtype=torch.int64, device=device)
-    d_cu = torch.empty(B + 1, dtype=torch.int32, device=device)
-    d_ctx = torch.empty((B, b0.ngram_size - 1), dtype=torch.int64, device=device)
-    out = torch.empty((L, T, H), dtype=torch.int64, device=device)
-    h_out = torch.empty((L, T, H), dtype=torch.int64).pin_memory()
+    slots = []
+    for _ in range(2):
+        slots.append(dict(
+            ids=torch.empty(T, dtype=torch.int64, device=device),
+            cu=torch.empty(B + 1, dtype=torch.int32, device=device),
+            ctx=torch.empty((B, b0.ngram_size - 1), dtype=torch.int64, device=device),
+            out=torch.empty((L, T, H), dtype=torch.int64, device=device),
+            h_out=torch.empty((L, T, H), dtype=torch.int64).pin_memory(),
+            computed=torch.cuda.Event(), copied=torch.cuda.Event()))
     steps = max(3, min(args.steps, 100))
     h2d = T * 8 + (B + 1) * 4 + B * (b0.ngram_size - 1) * 8
     d2h = L * T * H * 8
+    d2h_stream = torch.cuda.Stream(device)
 
-    def step(i):
-        h = host[i % len(host)]
-        d_ids.copy_(h["ids"], non_blocking=True)
-        d_cu.copy_(h["cu"], non_blocking=True)
-        d_ctx.copy_(h["ctx"], non_blocking=True)
-        ple.ple_row_ids(d_ids, None, None, d_ctx, M, vocab, off, b0.ngram_size,
-                        b0.heads_per_ngram, b0.boundary_id, out=out, cu_seqlens=d_cu)
-        h_out.copy_(out, non_blocking=True)
+    def run(i, pipelined):
+        h, sl = host[i % len(host)], slots[i % 2 if pipelined else 0]
+        if pipelined:
+            stream.wait_event(sl["copied"])  # the slot's previous rows are in host memory
+        sl["ids"].copy_(h["ids"], non_blocking=True)
+        sl["cu"].copy_(h["cu"], non_blocking=True)
+        sl["ctx"].copy_(h["ctx"], non_blocking=True)
+        ple.ple_row_ids(sl["ids"], None, None, sl["ctx"], M, vocab, off, b0.ngram_size,
+                        b0.heads_per_ngram, b0.boundary_id, out=sl["out"], cu_seqlens=sl["cu"])
+        if pipelined:
+            sl["computed"].record(stream)
+            d2h_stream.wait_event(sl["computed"])
+            with torch.cuda.stream(d2h_stream):
+                sl["h_out"].copy_(sl["out"], non_blocking=True)
+            sl["copied"].record(d2h_stream)
+        else:
+            sl["h_out"].copy_(sl["out"], non_blocking=True)
 
-    for i in range(3):
-        step(i)
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    ms = e0.elapsed_time(e1)
+    def timed(pipelined):
+        for i in range(3):
+            run(i, pipelined)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            run(i, pipelined)
+        if pipelined:
+            stream.wait_stream(d2h_stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1)
+
+    ms_serial = timed(False)
+    ms = timed(True)
     return {"value": b0.row_ids_per_call * steps / (ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps,
+            "method": "two buffer slots; each step's device-to-host copy overlaps the next "
+                      "step's host-to-device copy and kernel",
+            "serial_ms_per_step": ms_serial / steps,
+            "serial_value": b0.row_ids_per_call * steps / (ms_serial / 1e3)}
 
 
 def decode_latency(ple, torch, device):
