@@ -857,6 +857,44 @@ def test_floor_mod_routine_matches_cuda_remainder():
     assert np.array_equal(fast, expect)
 
 
+def test_floor_mod_fast_path_divisor_sweep():
+    """The 32-bit fast path (0 < v <= 2^29) over every divisor up to 2^16 and
+    20000 random ones up to 2^29 (plus the powers of two and their
+    neighbours, and the first divisors past 2^29, which take the general
+    path), each with dividends at the ends of the int64 range, at multiples
+    of v +- 1 near them, and with the offset-binary low word all ones (the
+    quotient estimate's dropped carries are largest there).  Expected values
+    from numpy's floored remainder, which takes the divisor's sign."""
+    rng = np.random.default_rng(7)
+    vs = np.concatenate([
+        np.arange(1, 2 ** 16 + 1, dtype=np.int64),
+        rng.integers(2 ** 16, 2 ** 29, size=20000, endpoint=True, dtype=np.int64),
+        np.array([2 ** k + d for k in range(1, 30) for d in (-1, 0, 1)] + [2 ** 29 + 2, 2 ** 30],
+                 dtype=np.int64)])
+    vs = vs[vs > 0]
+    lo_ones = np.int64(0xFFFFFFFF)
+    per_v = []
+    big = wl.I64_MAX // vs  # multiples of v near the ends
+    per_v.append(np.full_like(vs, wl.I64_MIN))
+    per_v.append(np.full_like(vs, wl.I64_MAX))
+    per_v.append(np.full_like(vs, -1))
+    per_v.append(np.zeros_like(vs))
+    for d in (-1, 0, 1):
+        per_v.append(big * vs + d if d <= 0 else big * vs - vs + d)
+        per_v.append(-big * vs + d)
+    hi = rng.integers(-(2 ** 31), 2 ** 31, size=vs.size, dtype=np.int64)
+    per_v.append((hi << 32) | lo_ones)          # low word all ones (offset binary too)
+    per_v.append((hi << 32) | lo_ones ^ (1 << 31))
+    per_v.append(rng.integers(wl.I64_MIN, wl.I64_MAX, size=vs.size, endpoint=True,
+                              dtype=np.int64))
+    x = np.concatenate(per_v)
+    v = np.tile(vs, len(per_v))
+    fast, ref = ple.ple_selftest_floor_mod(dev(x), dev(v))
+    fast = fast.cpu().numpy()
+    assert np.array_equal(fast, ref.cpu().numpy())
+    assert np.array_equal(fast, np.remainder(x, v))
+
+
 def test_stream_argument_is_honoured():
     batch = wl.ragged_16()
     s = torch.cuda.Stream(DEV)
