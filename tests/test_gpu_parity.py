@@ -9,6 +9,7 @@ workloads.py; expected values come from the oracle only.
 """
 
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -930,3 +931,64 @@ def test_binding_refuses_malformed_new_arguments():
     exp = oracle_rows(b)
     assert_same(ple.ple_row_ids(*args, heads=heads, cu_seqlens=dev(b.cu_seqlens)), exp,
                 "well-formed search mode with prepared constants")
+
+
+FUZZ_SHAPES = [(3, 2), (3, 4), (4, 4), (5, 8)]
+FUZZ_MODES = ["arrays", "arrays_i32", "search", "carry", "prepared", "index_free", "misaligned"]
+
+
+def fuzz_case(seed):
+    """One random call: the kernel (small-batch or tiled), the shape (a tuned
+    fixed shape 60% of the time, else random), the ids dtype, the vocab mix,
+    the way the index is given, the output dtype, the context carry and
+    prepared constants all drawn from the seed."""
+    rng = np.random.default_rng(seed)
+    kernel = "small" if seed % 2 else "tiled"
+    N, hpn = FUZZ_SHAPES[rng.integers(0, 4)] if rng.random() < 0.6 else (None, None)
+    b = wl.random_batch(seed, T_max=int(rng.choice([8, 64, 150, 400])), N=N, hpn=hpn,
+                        ids_dtype=np.int32 if rng.random() < 0.4 else np.int64,
+                        vocab_mode="primes" if rng.random() < 0.5 else "mixed")
+    if kernel == "small" and b.row_ids_per_call > ple.small_batch_max_rows():
+        kernel = "tiled"
+    b = for_kernel(b, kernel)
+    mode = str(rng.choice(FUZZ_MODES))
+    if mode == "index_free" and not b.is_decode:
+        mode = "search"
+    out_dtype = torch.int32 if rng.random() < 0.4 else torch.int64
+    carry, prepared = bool(rng.random() < 0.5), bool(rng.random() < 0.5)
+    nxt = None
+    if mode in ("arrays", "misaligned"):
+        out_dtype = torch.int64
+        out = None
+        if mode == "misaligned":
+            L, T, H = b.num_layers, b.num_tokens, b.num_heads
+            out = torch.full((L * T * H + 1,), 7, dtype=torch.int64, device=DEV)[1:].view(L, T, H)
+        got = gpu_rows(b, out=out)
+    elif mode == "arrays_i32":
+        out_dtype = torch.int32
+        req, local = gpu_index(b)
+        got = ple.ple_row_ids(dev(b.ids), req, local, dev(b.ngram_context),
+                              dev(b.layer_multipliers), dev(b.vocab_sizes), dev(b.offsets),
+                              b.ngram_size, b.heads_per_ngram, b.boundary_id, out_dtype=out_dtype)
+    elif mode == "search":
+        got, nxt = gpu_rows_search(b, out_dtype=out_dtype, carry=carry, prepared=prepared)
+    elif mode == "carry":
+        got, nxt = gpu_rows_carry(b, out_dtype=out_dtype)
+    elif mode == "prepared":
+        got, nxt = gpu_rows_prepared(b, out_dtype=out_dtype, carry=carry)
+    else:
+        got, nxt = gpu_rows_carry(b, out_dtype=out_dtype, index_free=True)
+    exp = oracle_rows(b)
+    what = f"fuzz seed {seed} ({kernel}, {mode})"
+    assert_same(got, low32(exp) if out_dtype == torch.int32 else exp, what)
+    if nxt is not None:
+        assert_same(nxt, oracle_carry(b), what + " carry")
+
+
+def test_random_call_fuzz():
+    """Random calls across every entry-point variant, each against the
+    oracle.  PLE_FUZZ_BATCHES sets how many (default 1500, a few seconds);
+    seeds are consecutive from 200000, so a failure names its seed."""
+    count = int(os.environ.get("PLE_FUZZ_BATCHES", "1500"))
+    for seed in range(200000, 200000 + count):
+        fuzz_case(seed)
