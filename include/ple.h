@@ -141,7 +141,8 @@ ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t num_requests
  * Errors: PLE_ERR_SIZE, PLE_ERR_GEOMETRY_CTX, PLE_ERR_GEOMETRY_HEADS (checked
  * in that order, before anything else), then PLE_ERR_NULL (one of req /
  * local NULL, or any other pointer), PLE_ERR_SIZE (both NULL with B != T),
- * PLE_ERR_DTYPE, PLE_ERR_ALIGN, PLE_ERR_CUDA.
+ * PLE_ERR_DTYPE, PLE_ERR_ALIGN, PLE_ERR_CUDA.  PLE_ERR_SIZE also when the
+ * output's byte count, L * T * H * 8, would not fit in int64.
  * One kernel launch; no host reads; the grid depends only on the sizes, the
  * way the index is given and the device (so a captured graph replays it).
  * Batches of at most ple_small_batch_max_rows() row ids (T * H * L) run the
@@ -279,7 +280,8 @@ ple_status ple_prepare_heads(const int64_t* vocab_sizes, const int64_t* offsets,
  *   heads         optional: constants from ple_prepare_heads, as in
  *                 ple_row_ids_ex (vocab_sizes and offsets may then be NULL).
  *
- * Errors: as ple_row_ids_ex, plus PLE_ERR_SIZE for dim / table_rows and
+ * Errors: as ple_row_ids_ex, plus PLE_ERR_SIZE for dim / table_rows or an
+ * output of more than INT64_MAX bytes (L * T * dim * 4), and
  * PLE_ERR_ALIGN for a table or out that is not 16-byte aligned.
  */
 ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_tokens,

@@ -95,6 +95,8 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     if ((int64_t)num_heads != (int64_t)(ngram_size - 1) * heads_per_ngram)
         return PLE_ERR_GEOMETRY_HEADS;
     if (num_heads > PLE_MAX_HEADS) return PLE_ERR_SIZE;
+    // the output's byte count, L * T * H int64, fits int64 (L * T < 2^62)
+    if ((int64_t)num_layers * num_tokens > (INT64_MAX / 8) / num_heads) return PLE_ERR_SIZE;
     if (num_tokens == 0) {
         *empty = true;
         return PLE_OK;
@@ -264,6 +266,8 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     if (dim < 8 || dim % 8 != 0 || dim > PLE_MAX_EMBED_DIM || table_rows < 0) return PLE_ERR_SIZE;
     // the table's byte size must fit in 64 bits
     if (table_rows > INT64_MAX / ((int64_t)num_layers * dim * 2)) return PLE_ERR_SIZE;
+    // the output's byte count, L * T * dim float, fits int64
+    if ((int64_t)num_layers * num_tokens > (INT64_MAX / 4) / dim) return PLE_ERR_SIZE;
     if (empty) return PLE_OK;
     if (!out || (table_rows > 0 && !table)) return PLE_ERR_NULL;
     if (!aligned(table, 16) || !aligned(out, 16)) return PLE_ERR_ALIGN;

@@ -73,6 +73,8 @@ def row_ids(lib, **kw):
     (dict(L=0), ple.PLE_ERR_SIZE),
     (dict(T=-1), ple.PLE_ERR_SIZE),
     (dict(T=2 ** 31), ple.PLE_ERR_SIZE),
+    (dict(T=2 ** 30, L=2 ** 30), ple.PLE_ERR_SIZE),          # L*T*H*8 bytes overflow int64
+    (dict(T=2 ** 28, L=2 ** 28, out=A + 4), ple.PLE_ERR_ALIGN),  # 2^61 bytes: past the size check
     (dict(ctx_len=3), ple.PLE_ERR_GEOMETRY_CTX),
     (dict(ctx_len=1), ple.PLE_ERR_GEOMETRY_CTX),
     (dict(H=5), ple.PLE_ERR_GEOMETRY_HEADS),
@@ -167,6 +169,8 @@ def row_embed(lib, **kw):
     (dict(D=65544), ple.PLE_ERR_SIZE),
     (dict(V=-1), ple.PLE_ERR_SIZE),
     (dict(V=2 ** 62), ple.PLE_ERR_SIZE),
+    (dict(T=2 ** 25, L=2 ** 25, D=65536, V=16), ple.PLE_ERR_SIZE),  # L*T*dim*4 bytes overflow
+    (dict(T=2 ** 22, L=2 ** 22, D=65536, V=16, out=A + 4), ple.PLE_ERR_ALIGN),  # 2^62 bytes fit
     (dict(table=None), ple.PLE_ERR_NULL),
     (dict(out=None), ple.PLE_ERR_NULL),
     (dict(table=A + 8), ple.PLE_ERR_ALIGN),
