@@ -742,15 +742,21 @@ def test_cu_search_mode_random_edges(chunk, kernel):
             assert_same(nxt, oracle_carry(batch), f"search carry {seed}")
 
 
+@pytest.mark.parametrize("B", [500, 600, 1000, 3000])
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_cu_search_mode_many_requests(kernel):
-    """Thousands of requests, many of them empty or one token long, so the
-    search runs a dozen steps and tiles span many requests."""
-    rng = np.random.default_rng(4321)
-    B = 3000 if kernel == "tiled" else 1000
+def test_cu_search_mode_many_requests(kernel, B):
+    """Hundreds to thousands of requests, many of them empty or one token
+    long, so a tile spans anywhere from one request to dozens: two rounds
+    of the warp's 32-way search (B = 500, 600, 1000) or three (B = 3000)."""
+    if kernel == "small" and B != 1000:
+        pytest.skip("the small-batch kernel has one search path")
+    rng = np.random.default_rng(4321 + B)
     lengths = rng.choice([0, 1, 1, 2, 5, 40], size=B)
+    if B in (500, 600):
+        lengths = rng.choice([0, 1, 2, 40, 100], size=B)
     T = int(lengths.sum())
-    base = wl.random_batch(99, N=4, hpn=4, L=1, T_max=10, decode_batch=False)
+    base = wl.random_batch(99, N=4, hpn=4, L=4 if B in (500, 600) else 1, T_max=10,
+                           decode_batch=False)
     batch = dataclasses.replace(
         base, ids=rng.integers(0, wl.VOCAB, size=T, dtype=np.int64),
         ngram_context=rng.integers(0, wl.VOCAB, size=(B, 3), dtype=np.int64),
@@ -795,13 +801,16 @@ def test_cu_search_mode_in_a_graph():
         assert_same(out, oracle_rows(nb), f"search-mode replay {replay}")
 
 
+@pytest.mark.parametrize("hpn", [2, 4])
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_cu_search_mode_malformed_cu_stays_in_bounds(kernel):
+def test_cu_search_mode_malformed_cu_stays_in_bounds(kernel, hpn):
     """cu_seqlens is device data the host cannot check.  Malformed contents
     (negative, past T, decreasing) give unspecified rows but no access
     outside the arrays: the canaries around the output and the carried
-    context survive, and the call completes."""
-    batch = for_kernel(wl.random_batch(5150, N=4, hpn=2, L=1, T_max=100, decode_batch=False),
+    context survive, and the call completes.  hpn = 4 is a fixed shape (the
+    warp search and lane ranking of the fixed-shape kernel), hpn = 2 a
+    runtime one (a per-lane search)."""
+    batch = for_kernel(wl.random_batch(5150, N=4, hpn=hpn, L=1, T_max=100, decode_batch=False),
                        kernel)
     L, T, H, B = batch.num_layers, batch.num_tokens, batch.num_heads, batch.num_requests
     rng = np.random.default_rng(3)
@@ -812,7 +821,7 @@ def test_cu_search_mode_malformed_cu_stays_in_bounds(kernel):
     nbuf = torch.full((B * 3 + 2,), 77, dtype=torch.int64, device=DEV)
     nxt = nbuf[1:-1].view(B, 3)
     ple.ple_row_ids(dev(batch.ids), None, None, ctx, dev(batch.layer_multipliers),
-                    dev(batch.vocab_sizes), dev(batch.offsets), 4, 2, batch.boundary_id, out=out,
+                    dev(batch.vocab_sizes), dev(batch.offsets), 4, hpn, batch.boundary_id, out=out,
                     cu_seqlens=dev(cu), next_context=nxt)
     torch.cuda.synchronize(DEV)
     assert int(buf[0]) == 0x5A5A and int(buf[-1]) == 0x5A5A
