@@ -996,8 +996,10 @@ def fuzz_case(seed):
 
 def test_random_call_fuzz():
     """Random calls across every entry-point variant, each against the
-    oracle.  PLE_FUZZ_BATCHES sets how many (default 1500, a few seconds);
-    seeds are consecutive from 200000, so a failure names its seed."""
+    oracle.  PLE_FUZZ_BATCHES sets how many (default 1500, a few seconds)
+    and PLE_FUZZ_SEED the first seed (default 200000); seeds are
+    consecutive, so a failure names its seed."""
     count = int(os.environ.get("PLE_FUZZ_BATCHES", "1500"))
-    for seed in range(200000, 200000 + count):
+    first = int(os.environ.get("PLE_FUZZ_SEED", "200000"))
+    for seed in range(first, first + count):
         fuzz_case(seed)
