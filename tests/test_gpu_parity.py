@@ -742,14 +742,12 @@ def test_cu_search_mode_random_edges(chunk, kernel):
             assert_same(nxt, oracle_carry(batch), f"search carry {seed}")
 
 
-@pytest.mark.parametrize("B", [500, 600, 1000, 3000])
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel,B", [("small", 1000), ("tiled", 500), ("tiled", 600),
+                                      ("tiled", 1000), ("tiled", 3000)])
 def test_cu_search_mode_many_requests(kernel, B):
     """Hundreds to thousands of requests, many of them empty or one token
     long, so a tile spans anywhere from one request to dozens: two rounds
     of the warp's 32-way search (B = 500, 600, 1000) or three (B = 3000)."""
-    if kernel == "small" and B != 1000:
-        pytest.skip("the small-batch kernel has one search path")
     rng = np.random.default_rng(4321 + B)
     lengths = rng.choice([0, 1, 1, 2, 5, 40], size=B)
     if B in (500, 600):
