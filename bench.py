@@ -1,31 +1,45 @@
 """Benchmark of the PLE n-gram row-id hash on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--shard]
 
 Prints ONE JSON line (rank 0).  A step is one pass of the whole hot path over
 one batch, through the C ABI: each token's (request, offset) found from
 cu_seqlens and the row-id hash of every layer, in one launch
-(ple_row_ids_ex with req = local = NULL and cu_seqlens).  The same step as
-two launches -- ple_build_token_index writing the index, then ple_row_ids
-reading it -- is timed beside it.  The
-workload is the large prefill: T=262144 tokens in 4 requests, ngram_size 4,
-4 heads per order (12 heads), 8 layers, int64 ids, 20% adversarial boundary
-runs.  Inputs are resident in HBM before the timed region; 64 distinct input
-sets rotate (256 MiB of inputs) and two output buffers alternate (201 MB of
-row ids written per step), so no step finds its inputs in the 126 MB L2.
+(ple_row_ids_ex with req = local = NULL and cu_seqlens).  The workload is the
+large prefill: T=262144 tokens in 4 requests, ngram_size 4, 4 heads per order
+(12 heads), 8 layers, int64 ids, 20% adversarial boundary runs.  Inputs are
+resident in HBM before the timed region; 64 distinct input sets rotate (256
+MiB of inputs) and two output buffers alternate (201 MB of row ids written
+per step), so no step finds its inputs in the 126 MB L2.
 
-Also measured, as extra keys: the row-id kernel's duration (the step's one
-launch, CUDA events on its stream) against the HBM roofline, the end-to-end
-rate with host buffers (pinned H2D of ids / cu_seqlens / context, the call,
-D2H of all row ids), the decode B=1 device time per call (a CUDA graph of 300
-calls, median of 7 replays), and the CPU oracle on the host cores.
+The timed region is exactly K steps back to back, bracketed by a barrier and
+a device synchronisation on both sides, with CUDA events at its ends on the
+launching stream.  It is repeated until at least --min-timed-ms of steps have
+been timed; the step time is the median over the repeats (their spread is
+reported), and the SM clocks are sampled across them.
+
+Also measured, as extra keys:
+  roofline     the step's one kernel against the HBM copy bandwidth;
+  configs      every workload of the path (the 512-token prefill, decode
+               B=1/4/8, the 16-request ragged prefill, the 48-layer mixed
+               batch in both index forms, the large prefill with int32 ids
+               and with int32 row ids, the fused table gather), device time
+               per call from CUDA graphs of back-to-back calls (median of 7
+               replays), each with its own clock record;
+  e2e          the same metric with host buffers (pinned H2D of the step's
+               inputs, D2H of its rows), and beside it the int32-row and
+               gather variants, which return fewer or different bytes;
+  decode_b1    device time per call, with and without programmatic
+               dependent launch;
+  cpu_baseline the CPU oracle on the host cores.
 
 --impl reference times the CPU oracle (the only reference this path has) on
 bounded samples of the same workload.
 
 Under torchrun (--gpus N > 1) every rank hashes its own seeded batch (weak
 scaling, no collective on the data path); the step time is the max over
-ranks.
+ranks.  With --shard the ranks split ONE batch by token range instead
+(ple_shard_plan / ple_shard_inputs: strong scaling, still no exchange).
 """
 
 from __future__ import annotations
@@ -83,8 +97,9 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def workload_config(batch: wl.Batch, extra=None):
-    cfg = {
+def workload_config(batch: wl.Batch):
+    """The workload, identical in both arms' lines."""
+    return {
         "workload": (f"{batch.name}: T={batch.num_tokens} in {batch.num_requests} requests, "
                      f"ngram_size={batch.ngram_size}, heads_per_ngram={batch.heads_per_ngram} "
                      f"(H={batch.num_heads}), L={batch.num_layers} layers, "
@@ -97,27 +112,42 @@ def workload_config(batch: wl.Batch, extra=None):
         "num_layers": batch.num_layers,
         "ids_dtype": batch.ids.dtype.name,
         "row_ids_per_step": batch.row_ids_per_call,
-        "launches_per_step": 2,
+        "launches_per_step": 1,
+        "step": "index found from cu_seqlens + row-id hash of every layer, one call",
     }
-    if extra:
-        cfg.update(extra)
-    return cfg
+
+
+def call_bytes(batch: wl.Batch, mode: str, out_bytes: int = 8, prepared: bool = False,
+               embed_dim: int = 0) -> int:
+    """Algorithmic bytes of one row-id (or gather) call: ids read, the index
+    read (mode "index"), cu_seqlens read (mode "cu"), nothing for a decode
+    without an index (mode "decode"), context and parameters read, row ids
+    written -- or, for the gather, the table rows read and the embeddings
+    written."""
+    idb = batch.ids.dtype.itemsize
+    T, B, L, H, N = (batch.num_tokens, batch.num_requests, batch.num_layers, batch.num_heads,
+                     batch.ngram_size)
+    index = {"index": 8 * T, "cu": 4 * (B + 1), "decode": 0}[mode]
+    params = 8 * L * N + (48 * L * H if prepared else 16 * L * H)
+    out = L * T * H * out_bytes if not embed_dim else L * T * H * embed_dim * 2 + L * T * embed_dim * 4
+    return T * idb + index + B * (N - 1) * idb + params + out
 
 
 # ---------------------------------------------------------------------------
-# clocks during the timed region
+# clocks during the timed regions
 
 
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: str):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.t_on = self.t_off = None
+        self.windows = {}
 
     def start(self):
         try:
@@ -134,34 +164,39 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.monotonic(), line.strip()))
 
-    def mark_on(self):
-        self.t_on = time.monotonic()
-
-    def mark_off(self):
-        self.t_off = time.monotonic()
+    def mark(self, name: str, on: bool):
+        w = self.windows.setdefault(name, [None, None])
+        w[0 if on else 1] = time.monotonic()
 
     def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def record(self, name: str):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "nvidia-smi unavailable"}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        t_on, t_off = self.windows.get(name, (None, None))
         rows = []
-        for t, line in self.lines:
+        for t, line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            rows.append((t, parts))
-        window = [r for t, r in rows if self.t_on and self.t_off and self.t_on <= t <= self.t_off]
-        used = window if window else [r for _, r in rows]
+            if len(parts) >= 9:
+                rows.append((t, parts))
+        window = [r for t, r in rows if t_on and t_off and t_on <= t <= t_off]
+        # a window shorter than the sampling period: the samples around it
+        if not window and t_on and t_off:
+            near = sorted(rows, key=lambda tr: min(abs(tr[0] - t_on), abs(tr[0] - t_off)))[:2]
+            used = [r for _, r in near]
+        else:
+            used = window
         sm = [float(r[1]) for r in used if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in used for i in range(4)
+        reasons = sorted({self.REASONS[i] for r in used for i in range(4)
                           if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
@@ -169,7 +204,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# distributed plumbing (weak scaling; no data-path collective)
+# distributed plumbing (no data-path collective)
 
 
 class Dist:
@@ -322,11 +357,10 @@ def reference_arm(args):
 
     def step(i):
         s = wl.slice_batch(batch, starts[i], starts[i] + n_tok)
-        req, local = oracle.token_index(s.cu_seqlens, s.num_requests, s.num_tokens, False)
         t = time.perf_counter()
+        req, local = oracle.token_index(s.cu_seqlens, s.num_requests, s.num_tokens, False)
         oracle.row_ids(s.ids, req, local, s.ngram_context, s.layer_multipliers, s.vocab_sizes,
                        s.offsets, s.ngram_size, s.heads_per_ngram, s.boundary_id)
-        oracle.token_index(s.cu_seqlens, s.num_requests, s.num_tokens, False)
         return time.perf_counter() - t, s.row_ids_per_call
 
     for i in range(args.warmup):
@@ -344,15 +378,81 @@ def reference_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
-        "config": workload_config(batch, {"reference": "CPU oracle (plain C, single thread), "
-                                                       "the only reference this path has",
-                                          "sample_tokens_per_step": n_tok}),
+        "config": workload_config(batch),
+        "config_notes": {"reference": "CPU oracle (plain C, single thread), the only "
+                                      "reference this path has",
+                         "sample_tokens_per_step": n_tok},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample, "host_cores": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# device timing helpers
+
+
+def graph_us_per_call(torch, device, calls_fns, calls: int, replays: int = 7):
+    """Median device µs per call of a CUDA graph of `calls` back-to-back calls
+    (cycling over calls_fns), over `replays` replays after one warm replay:
+    the page's 7 x 300 method.  Returns (median, runs)."""
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for fn in calls_fns:
+            fn()
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(calls):
+            calls_fns[i % len(calls_fns)]()
+    g.replay()
+    torch.cuda.synchronize(device)
+    runs = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(device)
+        runs.append(1e3 * e0.elapsed_time(e1) / calls)
+    del g
+    return statistics.median(runs), runs
+
+
+def timed_regions(torch, device, stream, dist, step, first: int, steps: int, min_ms: float,
+                  max_regions: int = 5000):
+    """Repeats the timed region -- exactly `steps` steps back to back,
+    bracketed by a barrier and a device synchronisation on both sides, CUDA
+    events at its ends on the launching stream -- until min_ms of steps have
+    been timed.  Returns the per-region milliseconds (max over ranks)."""
+    out, total, i = [], 0.0, first
+    while (total < min_ms or len(out) < 3) and len(out) < max_regions:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(steps):
+            step(i)
+            i += 1
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        dist.barrier()
+        ms = dist.max(e0.elapsed_time(e1), device)
+        out.append(ms)
+        total += ms
+    return out
+
+
+def spread(per_step_ms):
+    a = np.asarray(per_step_ms)
+    return {"regions": int(a.size), "median": float(np.median(a)), "min": float(a.min()),
+            "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "max": float(a.max())}
 
 
 # ---------------------------------------------------------------------------
@@ -374,8 +474,9 @@ def our_arm(args):
     sh = ctypes.c_void_p(stream.cuda_stream)
 
     # ---- inputs, resident in HBM: ROTATE seeded batches sharing the model's parameters
-    base = wl.prefill_262144(replay=1000 * dist.rank)
-    batches = [base] + [wl.prefill_262144(replay=1000 * dist.rank + r) for r in range(1, ROTATE)]
+    seed0 = 0 if args.shard else 1000 * dist.rank
+    base = wl.prefill_262144(replay=seed0)
+    batches = [base] + [wl.prefill_262144(replay=seed0 + r) for r in range(1, ROTATE)]
     T, B, N, hpn, L, H = (base.num_tokens, base.num_requests, base.ngram_size,
                           base.heads_per_ngram, base.num_layers, base.num_heads)
 
@@ -383,32 +484,58 @@ def our_arm(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
     M, vocab, off = to_dev(base.layer_multipliers), to_dev(base.vocab_sizes), to_dev(base.offsets)
+    P = ctypes.c_void_p
+    C = N - 1
+    if args.shard:
+        # one batch split by token range over the ranks: this rank's share
+        plans = [ple.ple_shard_plan(b.cu_seqlens, B, T, dist.world, dist.rank) for b in batches]
+        span = max(p[1] - p[0] for p in plans)
     sets = []
     for b in batches:
-        sets.append(dict(ids=to_dev(b.ids), ctx=to_dev(b.ngram_context), cu=to_dev(b.cu_seqlens),
-                         req=torch.empty(T, dtype=torch.int32, device=device),
-                         local=torch.empty(T, dtype=torch.int32, device=device)))
-    outs = [torch.empty((L, T, H), dtype=torch.int64, device=device) for _ in range(2)]
-    P = ctypes.c_void_p
-    idx_args, row_args, search_args = [], [], []
+        s = dict(ids=to_dev(b.ids), ctx=to_dev(b.ngram_context), cu=to_dev(b.cu_seqlens),
+                 req=torch.empty(T, dtype=torch.int32, device=device),
+                 local=torch.empty(T, dtype=torch.int32, device=device))
+        if args.shard:
+            s["scu"] = torch.empty(B + 1, dtype=torch.int32, device=device)
+            s["sctx"] = torch.empty((B, C), dtype=torch.int64, device=device)
+        sets.append(s)
+    T_out = span if args.shard else T
+    outs = [torch.empty((L, T_out, H), dtype=torch.int64, device=device) for _ in range(2)]
+    idx_args, row_args, search_args, shard_args = [], [], [], []
     for k, s in enumerate(sets):
         idx_args.append((P(s["cu"].data_ptr()), B, T, 0, P(s["req"].data_ptr()),
                          P(s["local"].data_ptr()), sh))
         row_args.append((P(s["ids"].data_ptr()), ple.PLE_I64, T, P(s["req"].data_ptr()),
-                         P(s["local"].data_ptr()), P(s["ctx"].data_ptr()), B, N - 1,
+                         P(s["local"].data_ptr()), P(s["ctx"].data_ptr()), B, C,
                          P(M.data_ptr()), P(vocab.data_ptr()), P(off.data_ptr()), H, N, hpn, L,
                          base.boundary_id, P(outs[k % 2].data_ptr()), sh))
         # the whole step in one launch: req = local = NULL with cu_seqlens,
         # each token's request found in the kernel
         search_args.append((P(s["ids"].data_ptr()), ple.PLE_I64, T, None, None,
-                            P(s["ctx"].data_ptr()), B, N - 1, P(M.data_ptr()),
+                            P(s["ctx"].data_ptr()), B, C, P(M.data_ptr()),
                             P(vocab.data_ptr()), P(off.data_ptr()), H, N, hpn, L,
                             base.boundary_id, P(outs[k % 2].data_ptr()), ple.PLE_I64,
                             P(s["cu"].data_ptr()), None, None, sh))
+        if args.shard:
+            tb, te, rb, rc = plans[k]
+            shard_args.append((
+                (P(s["ids"].data_ptr()), ple.PLE_I64, P(s["cu"].data_ptr()),
+                 P(s["ctx"].data_ptr()), B, T, C, tb, te, rb, rc, P(s["scu"].data_ptr()),
+                 P(s["sctx"].data_ptr()), sh),
+                (P(s["ids"].data_ptr() + 8 * tb), ple.PLE_I64, te - tb, None, None,
+                 P(s["sctx"].data_ptr()), rc, C, P(M.data_ptr()), P(vocab.data_ptr()),
+                 P(off.data_ptr()), H, N, hpn, L, base.boundary_id, P(outs[k % 2].data_ptr()),
+                 ple.PLE_I64, P(s["scu"].data_ptr()), None, None, sh)))
     f_idx, f_rows, f_search = lib.ple_build_token_index, lib.ple_row_ids, lib.ple_row_ids_ex
+    f_shard = lib.ple_shard_inputs
 
     def step(i):
         if f_search(*search_args[i % ROTATE]):
+            raise RuntimeError("library call failed")
+
+    def step_shard(i):
+        a, r = shard_args[i % ROTATE]
+        if f_shard(*a) | f_search(*r):
             raise RuntimeError("library call failed")
 
     def step_with_index(i):
@@ -417,94 +544,118 @@ def our_arm(args):
         if st:
             raise RuntimeError(f"library call failed: status {st}")
 
+    main_step = step_shard if args.shard else step
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     clocks = ClockSampler(visible.split(",")[dist.local_rank].strip() if visible else
                           str(dist.local_rank))
     clocks.start()
     for i in range(args.warmup):
-        step(i)
-        step_with_index(i)
+        main_step(i)
+        if not args.shard:
+            step_with_index(i)
     torch.cuda.synchronize(device)
 
-    # ---- the timed region: K steps back to back, events only at its ends
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize(device)
-    clocks.mark_on()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
-    t_end.record(stream)
-    torch.cuda.synchronize(device)
-    dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
+    # ---- the timed regions: K steps back to back each, repeated
+    clocks.mark("headline", True)
+    regions = timed_regions(torch, device, stream, dist, main_step, args.warmup, args.steps,
+                            args.min_timed_ms)
+    clocks.mark("headline", False)
+    per_step = [ms / args.steps for ms in regions]
+    step_ms = statistics.median(per_step)
+    clk = clocks.record("headline")
 
     # ---- the step as two launches (ple_build_token_index, then ple_row_ids
-    # reading the index), K steps back to back, for comparison
-    w_start = torch.cuda.Event(enable_timing=True)
-    w_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(device)
-    w_start.record(stream)
-    for i in range(args.steps):
-        step_with_index(args.warmup + i)
-    w_end.record(stream)
-    torch.cuda.synchronize(device)
-    with_index_ms = w_start.elapsed_time(w_end) / args.steps
-    # the step's one kernel with an event pair around every launch, for
-    # reference (an event between launches serialises them and adds its own
-    # drain-and-launch gap to every launch)
-    n_br = min(args.steps, 200)
-    br = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n_br)]
-    for i in range(n_br):
-        br[i][0].record(stream)
-        step(i)
-        br[i][1].record(stream)
-    torch.cuda.synchronize(device)
-    clocks.mark_off()
-    bracketed_ms = float(np.median([a.elapsed_time(b) for a, b in br]))
-    # the step is one launch, so the dominant kernel's average duration is the
-    # step's, measured over the timed region on the launching stream
-    kern_avg_ms = total_ms / args.steps
-    total_ms = dist.max(total_ms, device)
-    clk = clocks.stop()
+    # reading the index), for comparison
+    with_index = None
+    bracketed_ms = None
+    if not args.shard:
+        w_regions = timed_regions(torch, device, stream, dist, step_with_index, args.warmup,
+                                  args.steps, args.min_timed_ms / 4)
+        with_index_ms = statistics.median([ms / args.steps for ms in w_regions])
+        with_index = {
+            "launches": 2, "ms_per_step": with_index_ms,
+            "value": dist.world * base.row_ids_per_call / (with_index_ms / 1e3), "unit": UNIT,
+            "what": "ple_build_token_index then ple_row_ids reading the index, back to back",
+            "timed_regions": len(w_regions)}
+        # the step's one kernel with an event pair around every launch, for
+        # reference (an event between launches serialises them and adds its
+        # own drain-and-launch gap to every launch)
+        n_br = 200
+        br = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_br)]
+        for i in range(n_br):
+            br[i][0].record(stream)
+            step(i)
+            br[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        bracketed_ms = float(np.median([a.elapsed_time(b) for a, b in br]))
 
-    rows_per_step = base.row_ids_per_call
-    value = dist.world * rows_per_step * args.steps / (total_ms / 1e3)
-    idb = base.ids.dtype.itemsize
-    # ids and cu_seqlens read, context and parameters read, row ids written
-    kernel_bytes = (T * (idb + 8 * L * H) + 4 * (B + 1) + B * (N - 1) * idb +
-                    8 * L * (N + 2 * H))
+    rows_total = base.row_ids_per_call if args.shard else dist.world * base.row_ids_per_call
+    value = rows_total / (step_ms / 1e3)
     peaks, peak_kind = measured_peaks()
-    achieved = kernel_bytes / (kern_avg_ms / 1e3) / 1e9
-    traffic = None
-    try:
-        with open(PROFILE_TRAFFIC) as fh:
-            prof = json.load(fh)
-        if prof.get("kernel_source_sha256_16") == kernel_source_hash():
-            traffic = prof.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "kernel": "ple row_ids kernel (row_ids_fixed_kernel<int64, 4, 4>, requests "
-                          "found from cu_seqlens in the kernel)",
-                "algorithmic_bytes_per_launch": kernel_bytes,
-                "kernel_ms_avg": kern_avg_ms,
-                "kernel_timing": f"the timed region: {args.steps} one-launch steps back to back, "
-                                 "CUDA events at its ends, on the launching stream",
-                "kernel_ms_bracketed_median": bracketed_ms,
-                "peak_kind": peak_kind}
+    if args.shard:
+        kernel_bytes = None
+        roofline = None
+    else:
+        # ids and cu_seqlens read, context and parameters read, row ids written
+        kernel_bytes = call_bytes(base, "cu")
+        achieved = kernel_bytes / (step_ms / 1e3) / 1e9
+        traffic = None
+        try:
+            with open(PROFILE_TRAFFIC) as fh:
+                prof = json.load(fh)
+            if prof.get("kernel_source_sha256_16") == kernel_source_hash():
+                traffic = prof.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            pass
+        sm_med = clk.get("sm_mhz")
+        roofline = {
+            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "kernel": "ple row_ids kernel (row_ids_fixed_kernel<int64, 4, 4>, requests found "
+                      "from cu_seqlens in the kernel)",
+            "algorithmic_bytes_per_launch": kernel_bytes,
+            "kernel_ms_avg": step_ms,
+            "kernel_timing": f"median over {len(regions)} timed regions of {args.steps} "
+                             "one-launch steps back to back, CUDA events at each region's ends "
+                             "on the launching stream",
+            "kernel_ms_bracketed_median": bracketed_ms,
+            "kernel_ms_x_sm_mhz": step_ms * sm_med if sm_med else None,
+            "peak_kind": peak_kind}
 
-    # ---- end to end through the public Python API with host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = end_to_end(args, ple, torch, device, stream, batches[:4], M, vocab, off)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "strong" if args.shard else "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": workload_config(base),
+        "config_notes": {
+            "l2": f"inputs rotate over {ROTATE} seeded sets ({ROTATE * (T * 16 + 64) >> 20} MiB) "
+                  f"and 2 output buffers ({L * T * H * 8 / 1e6:.0f} MB written per step); "
+                  "no step's data fits the 126 MB L2",
+            "parallelism": (f"token-range shards x{dist.world} of one batch (ple_shard_plan + "
+                            "ple_shard_inputs + the row-id call per rank; no collective)"
+                            if args.shard else
+                            f"replicas x{dist.world} (weak scaling, no collective)")},
+        "timed_regions": spread(per_step),
+        "roofline": roofline,
+        "gpu_launches": args.steps * (2 if args.shard else 1),
+        "gpu_launches_note": "per timed region (each region is exactly --steps steps)",
+        "step_with_index_build": with_index,
+        "clocks": clk,
+    }
 
-    decode = None if args.no_decode else decode_latency(ple, torch, device)
+    if dist.world == 1 and not args.shard:
+        if not args.no_configs:
+            line["configs"] = all_configs(args, ple, torch, device, clocks, peaks)
+        if not args.no_e2e:
+            line["e2e"] = end_to_end(args, ple, torch, device, stream, batches[:4], M, vocab, off)
+            line["e2e_variants"] = e2e_variants(args, ple, torch, device, stream, batches[:4],
+                                                M, vocab, off)
+        if not args.no_decode:
+            line["decode_b1"] = decode_latency(ple, torch, device)
+    clocks.stop()
 
-    cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -524,35 +675,14 @@ def our_arm(args):
                     "sample": f"{cores} processes at once, each hashing a {sample.num_tokens}-token "
                               f"slice of {base.name} (index + row ids) for about "
                               f"{min(8.0, args.cpu_budget):.0f} s"}
-
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-        "config": workload_config(base, {
-            "l2": f"inputs rotate over {ROTATE} seeded sets ({ROTATE * (T * 16 + 64) >> 20} MiB) "
-                  f"and 2 output buffers ({L * T * H * 8 / 1e6:.0f} MB written per step); "
-                  "no step's data fits the 126 MB L2",
-            "parallelism": f"replicas x{dist.world} (weak scaling, no collective)"}),
-        "roofline": roofline,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": args.steps,
-        "step": "one launch: ple_row_ids_ex with req = local = NULL and cu_seqlens",
-        "step_with_index_build": {
-            "launches": 2, "ms_per_step": with_index_ms,
-            "value": dist.world * rows_per_step / (with_index_ms / 1e3), "unit": UNIT,
-            "what": "ple_build_token_index then ple_row_ids reading the index, back to back"},
-        "clocks": clk,
-        "decode_b1": decode,
-    }
+        line["cpu_baseline"] = cpu
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
     return 0
 
 
-def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
+def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off, out_dtype=None):
     """The same metric through ple_row_ids (the Python binding; requests
     found from cu_seqlens in the kernel) with host buffers: every step copies
     its ids, cu_seqlens and context from pinned host memory, runs the call,
@@ -564,6 +694,7 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
     slot is reused only after its previous copy back has finished.  The
     timed region ends when the last step's rows are in host memory.  The
     same steps run one after another on one stream are reported beside it."""
+    out_dtype = out_dtype or torch.int64
     b0 = batches[0]
     T, B, L, H = b0.num_tokens, b0.num_requests, b0.num_layers, b0.num_heads
     host = []
@@ -577,12 +708,12 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
             ids=torch.empty(T, dtype=torch.int64, device=device),
             cu=torch.empty(B + 1, dtype=torch.int32, device=device),
             ctx=torch.empty((B, b0.ngram_size - 1), dtype=torch.int64, device=device),
-            out=torch.empty((L, T, H), dtype=torch.int64, device=device),
-            h_out=torch.empty((L, T, H), dtype=torch.int64).pin_memory(),
+            out=torch.empty((L, T, H), dtype=out_dtype, device=device),
+            h_out=torch.empty((L, T, H), dtype=out_dtype).pin_memory(),
             computed=torch.cuda.Event(), copied=torch.cuda.Event()))
     steps = max(3, min(args.steps, 100))
     h2d = T * 8 + (B + 1) * 4 + B * (b0.ngram_size - 1) * 8
-    d2h = L * T * H * 8
+    d2h = L * T * H * slots[0]["out"].element_size()
     d2h_stream = torch.cuda.Stream(device)
 
     def run(i, pipelined):
@@ -593,7 +724,8 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
         sl["cu"].copy_(h["cu"], non_blocking=True)
         sl["ctx"].copy_(h["ctx"], non_blocking=True)
         ple.ple_row_ids(sl["ids"], None, None, sl["ctx"], M, vocab, off, b0.ngram_size,
-                        b0.heads_per_ngram, b0.boundary_id, out=sl["out"], cu_seqlens=sl["cu"])
+                        b0.heads_per_ngram, b0.boundary_id, out=sl["out"], cu_seqlens=sl["cu"],
+                        out_dtype=out_dtype)
         if pipelined:
             sl["computed"].record(stream)
             d2h_stream.wait_event(sl["computed"])
@@ -622,10 +754,66 @@ def end_to_end(args, ple, torch, device, stream, batches, M, vocab, off):
     return {"value": b0.row_ids_per_call * steps / (ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
+            "row_ids_dtype": str(out_dtype).replace("torch.", ""),
             "method": "two buffer slots; each step's device-to-host copy overlaps the next "
                       "step's host-to-device copy and kernel",
             "serial_ms_per_step": ms_serial / steps,
             "serial_value": b0.row_ids_per_call * steps / (ms_serial / 1e3)}
+
+
+def e2e_variants(args, ple, torch, device, stream, batches, M, vocab, off):
+    """End to end for the variants that return fewer bytes: int32 row ids
+    (half the device-to-host bytes), and the fused gather, whose result is the
+    embeddings ([L, T, D] fp32, D = --embed-dim) instead of row ids."""
+    res = {"int32_row_ids": end_to_end(args, ple, torch, device, stream, batches, M, vocab, off,
+                                       out_dtype=torch.int32)}
+    b0 = batches[0]
+    T, B, L, H, N = b0.num_tokens, b0.num_requests, b0.num_layers, b0.num_heads, b0.ngram_size
+    D = args.embed_dim
+    V = int(b0.vocab_sizes.sum(axis=1).max())
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4000)
+    table = torch.randn((L, V, D), dtype=torch.bfloat16, device=device, generator=gen)
+    host = [dict(ids=torch.from_numpy(b.ids).pin_memory(),
+                 cu=torch.from_numpy(b.cu_seqlens).pin_memory(),
+                 ctx=torch.from_numpy(np.ascontiguousarray(b.ngram_context)).pin_memory())
+            for b in batches]
+    ids = torch.empty(T, dtype=torch.int64, device=device)
+    cu = torch.empty(B + 1, dtype=torch.int32, device=device)
+    ctx = torch.empty((B, N - 1), dtype=torch.int64, device=device)
+    out = torch.empty((L, T, D), dtype=torch.float32, device=device)
+    h_out = torch.empty((L, T, D), dtype=torch.float32).pin_memory()
+
+    def run(i):
+        h = host[i % len(host)]
+        ids.copy_(h["ids"], non_blocking=True)
+        cu.copy_(h["cu"], non_blocking=True)
+        ctx.copy_(h["ctx"], non_blocking=True)
+        ple.ple_row_embed(ids, None, None, ctx, M, vocab, off, N, b0.heads_per_ngram,
+                          b0.boundary_id, table, out=out, cu_seqlens=cu)
+        h_out.copy_(out, non_blocking=True)
+
+    for i in range(2):
+        run(i)
+    torch.cuda.synchronize(device)
+    steps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        run(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    res["row_embed"] = {
+        "value": L * T / (ms / 1e3), "unit": "embeddings/s", "ms_per_step": ms, "steps": steps,
+        "h2d_bytes_per_step": T * 8 + (B + 1) * 4 + B * (N - 1) * 8,
+        "d2h_bytes_per_step": L * T * D * 4,
+        "row_ids_per_s_equivalent": b0.row_ids_per_call / (ms / 1e3),
+        "method": f"one stream: H2D of ids / cu_seqlens / context, ple_row_embed (D={D}, bf16 "
+                  f"table of {L * V * D * 2 / 1e9:.1f} GB resident), D2H of every embedding"}
+    del table
+    torch.cuda.empty_cache()
+    return res
 
 
 def decode_latency(ple, torch, device):
@@ -634,7 +822,9 @@ def decode_latency(ple, torch, device):
     Measured without an index (req = local = NULL, one launch per step) and
     with a prebuilt index (the page's memoized index), each with the head
     constants derived in the call (the page's arguments) and prepared once
-    by ple_prepare_heads (model parameters, fixed across steps)."""
+    by ple_prepare_heads (model parameters, fixed across steps); and without
+    an index with programmatic dependent launch off, so that no call's launch
+    overlaps the one before it."""
     b = wl.decode(1)
 
     def to_dev(a):
@@ -646,46 +836,133 @@ def decode_latency(ple, torch, device):
     heads = ple.ple_prepare_heads(vocab, off)
     out = torch.empty((1, 1, 4), dtype=torch.int64, device=device)
     res = {"launches_per_call": 1, "method": "CUDA graph of 300 calls, median of 7 replays"}
-    for name, (rq, lc, hd) in (("device_us_per_call", (None, None, None)),
-                               ("device_us_per_call_with_index", (req, local, None)),
-                               ("device_us_per_call_prepared_heads", (None, None, heads)),
-                               ("device_us_per_call_with_index_prepared_heads",
-                                (req, local, heads))):
+    for name, (rq, lc, hd, pdl) in (
+            ("device_us_per_call", (None, None, None, True)),
+            ("device_us_per_call_with_index", (req, local, None, True)),
+            ("device_us_per_call_prepared_heads", (None, None, heads, True)),
+            ("device_us_per_call_with_index_prepared_heads", (req, local, heads, True)),
+            ("device_us_per_call_no_programmatic_launch", (None, None, None, False)),
+            ("device_us_per_call_prepared_heads_no_programmatic_launch",
+             (None, None, heads, False))):
         def call():
             ple.ple_row_ids(ids, rq, lc, ctx, M, vocab, off, 3, 2, b.boundary_id, out=out,
                             heads=hd)
 
-        s = torch.cuda.Stream(device)
-        s.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(s):
-            call()
-        torch.cuda.current_stream(device).wait_stream(s)
-        torch.cuda.synchronize(device)
-        g = torch.cuda.CUDAGraph()
-        calls = 300
-        with torch.cuda.graph(g):
-            for _ in range(calls):
-                call()
-        g.replay()
-        torch.cuda.synchronize(device)
-        per_call = []
-        for _ in range(7):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            g.replay()
-            e1.record()
-            torch.cuda.synchronize(device)
-            per_call.append(1e3 * e0.elapsed_time(e1) / calls)
-        res[name] = statistics.median(per_call)
+        prev = ple.set_programmatic_launch(pdl)
+        try:
+            us, runs = graph_us_per_call(torch, device, [call], 300)
+        finally:
+            ple.set_programmatic_launch(prev)
+        res[name] = us
         if name == "device_us_per_call":
-            res["runs_us"] = per_call
+            res["runs_us"] = runs
     return res
 
 
-def all_configs(args):
-    """Every workload: device time per call of ple_row_ids and of a whole
-    step (index + row ids), each from a CUDA graph of 300 back-to-back calls,
-    median of 7 replays (the page's 7 x 300 method); one JSON object."""
+def all_configs(args, ple, torch, device, clocks, peaks):
+    """Every workload of the path, device µs per call from a CUDA graph of
+    back-to-back calls, median of 7 replays (the page's 7 x 300 method), each
+    with the clocks sampled while it ran.  Workloads whose data fits in L2
+    reuse one input set (as the page's method does); the large ones cycle
+    over 16 input sets (ids rolled) and two output buffers."""
+    entries = {}
+    hbm = peaks["hbm_gbs"]
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    def entry(key, batch, variants, sets=1):
+        """variants: (name, mode, out_dtype, prepared, index_build, pdl)."""
+        if args.only and key not in args.only:
+            return
+        T, B, L, H = batch.num_tokens, batch.num_requests, batch.num_layers, batch.num_heads
+        M, vocab, off = (to_dev(batch.layer_multipliers), to_dev(batch.vocab_sizes),
+                         to_dev(batch.offsets))
+        heads = ple.ple_prepare_heads(vocab, off)
+        ins = []
+        for r in range(sets):
+            ids = batch.ids if r == 0 else np.roll(batch.ids, 977 * r)
+            d = dict(ids=to_dev(ids), ctx=to_dev(batch.ngram_context),
+                     cu=to_dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None)
+            d["req"], d["local"] = ple.ple_build_token_index(d["cu"], B, T, batch.is_decode,
+                                                             device=device)
+            ins.append(d)
+        res = {"workload": batch.name, "T": T, "B": B, "L": L, "H": H,
+               "ngram_size": batch.ngram_size, "ids_dtype": batch.ids.dtype.name,
+               "row_ids_per_call": batch.row_ids_per_call}
+        calls = 300
+        for name, mode, odt, prepared, build_index, pdl in variants:
+            outs = [torch.empty((L, T, H), dtype=odt, device=device)
+                    for _ in range(2 if sets > 1 else 1)]
+            fns = []
+            for r, d in enumerate(ins):
+                o = outs[r % len(outs)]
+
+                def fn(d=d, o=o):
+                    if build_index:
+                        ple.ple_build_token_index(d["cu"], B, T, batch.is_decode, req=d["req"],
+                                                  local=d["local"])
+                    idx = mode == "index"
+                    ple.ple_row_ids(d["ids"], d["req"] if idx else None,
+                                    d["local"] if idx else None, d["ctx"], M, vocab, off,
+                                    batch.ngram_size, batch.heads_per_ngram, batch.boundary_id,
+                                    out=o, out_dtype=odt, heads=heads if prepared else None,
+                                    cu_seqlens=d["cu"] if mode == "cu" else None)
+                fns.append(fn)
+            prev = ple.set_programmatic_launch(pdl)
+            clocks.mark(key + name, True)
+            try:
+                us, _ = graph_us_per_call(torch, device, fns, calls)
+            finally:
+                clocks.mark(key + name, False)
+                ple.set_programmatic_launch(prev)
+            nb = call_bytes(batch, mode, 4 if odt == torch.int32 else 8, prepared)
+            v = {"us_per_call": us, "launches_per_call": 2 if build_index else 1,
+                 "row_ids_per_s": batch.row_ids_per_call / (us / 1e6),
+                 "clocks": clocks.record(key + name)}
+            if not build_index:
+                v["algorithmic_bytes"] = nb
+                v["achieved_gbs"] = nb / (us / 1e6) / 1e9
+                v["frac_of_measured_hbm"] = v["achieved_gbs"] / hbm
+            res[name] = v
+        res["method"] = (f"CUDA graph of {calls} back-to-back calls over {sets} input set(s), "
+                         "median of 7 replays")
+        entries[key] = res
+        print(json.dumps({key: res}), file=sys.stderr, flush=True)
+
+    I64, I32 = torch.int64, torch.int32
+    # (name, mode, out dtype, prepared heads, index build in the call, programmatic launch)
+    one = ("one_launch", "cu", I64, False, False, True)
+    two = ("two_launch_step", "index", I64, False, True, True)
+    idx = ("row_ids_reading_index", "index", I64, False, False, True)
+    entry("prefill_512", wl.prefill_512(), [one, two, idx])
+    for Bd in (1, 4, 8):
+        entry(f"decode_b{Bd}", wl.decode(Bd), [
+            ("one_launch", "decode", I64, False, False, True),
+            ("one_launch_prepared_heads", "decode", I64, True, False, True),
+            ("one_launch_no_programmatic_launch", "decode", I64, False, False, False),
+            ("two_launch_step", "index", I64, False, True, True)])
+    entry("ragged_16", wl.ragged_16(), [one, two, idx])
+    entry("mixed_8192", wl.mixed_8192(), [
+        one, idx, two,
+        ("one_launch_prepared_heads", "cu", I64, True, False, True),
+        ("row_ids_reading_index_prepared_heads", "index", I64, True, False, True),
+        ("one_launch_int32_row_ids", "cu", I32, False, False, True)], sets=16)
+    entry("prefill_262144_int32_ids", wl.prefill_262144(ids_dtype=np.int32), [one], sets=16)
+    entry("prefill_262144_int32_row_ids", wl.prefill_262144(), [
+        ("one_launch", "cu", I32, False, False, True),
+        ("row_ids_reading_index", "index", I32, False, False, True)], sets=16)
+    if not args.no_embed:
+        for b in (wl.prefill_262144(), wl.prefill_262144_lowrep()):
+            if not args.only or "row_embed_" + b.name in args.only:
+                entries["row_embed_" + b.name] = embed_entry(args, ple, torch, device, clocks,
+                                                             b, peaks)
+    return entries
+
+
+def configs_only(args):
+    """Only the per-workload figures (all, or --only KEY ...), one JSON
+    object; a small process for profiling one workload's kernels."""
     import torch
 
     import layer_gram_embedding_gb300 as ple
@@ -694,123 +971,26 @@ def all_configs(args):
     lib_build.build()
     device = torch.device("cuda", 0)
     peaks, _ = measured_peaks()
-    out = []
-    for batch in wl.all_workloads():
-        wname = batch.name + ("_i32" if batch.ids.dtype == np.int32 else "")
-        if args.only and wname not in args.only:
-            continue
-
-        def to_dev(a):
-            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
-
-        T, B, L, H = batch.num_tokens, batch.num_requests, batch.num_layers, batch.num_heads
-        ids, ctx = to_dev(batch.ids), to_dev(batch.ngram_context)
-        M, vocab, off = (to_dev(batch.layer_multipliers), to_dev(batch.vocab_sizes),
-                         to_dev(batch.offsets))
-        cu = to_dev(batch.cu_seqlens) if batch.cu_seqlens is not None else None
-        req = torch.empty(T, dtype=torch.int32, device=device)
-        local = torch.empty(T, dtype=torch.int32, device=device)
-        o = torch.empty((L, T, H), dtype=torch.int64, device=device)
-        o32 = torch.empty((L, T, H), dtype=torch.int32, device=device)
-        # the row-id variants read a built index, as a serving step would
-        ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
-
-        def rows():
-            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
-                            batch.heads_per_ngram, batch.boundary_id, out=o)
-
-        def rows_i32():
-            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
-                            batch.heads_per_ngram, batch.boundary_id, out=o32,
-                            out_dtype=torch.int32)
-
-        def rows_no_index():
-            ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, batch.ngram_size,
-                            batch.heads_per_ngram, batch.boundary_id, out=o)
-
-        heads = ple.ple_prepare_heads(vocab, off)
-
-        def rows_prepared():
-            ple.ple_row_ids(ids, req, local, ctx, M, vocab, off, batch.ngram_size,
-                            batch.heads_per_ngram, batch.boundary_id, out=o, heads=heads)
-
-        def one_launch_step():
-            # no index: a prefill's requests found from cu_seqlens in the
-            # kernel, a decode's synthesised (req = t, local = 0)
-            ple.ple_row_ids(ids, None, None, ctx, M, vocab, off, batch.ngram_size,
-                            batch.heads_per_ngram, batch.boundary_id, out=o, cu_seqlens=cu)
-
-        def step():
-            ple.ple_build_token_index(cu, B, T, batch.is_decode, req=req, local=local)
-            rows()
-
-        res = {"workload": wname,
-               "T": T, "B": B, "L": L, "H": H, "ngram_size": batch.ngram_size,
-               "row_ids_per_call": batch.row_ids_per_call,
-               "algorithmic_bytes": batch.algorithmic_bytes(), "launches_per_call": 1}
-        variants = [("row_ids", rows), ("step", step), ("step_one_launch", one_launch_step),
-                    ("row_ids_i32", rows_i32), ("row_ids_prepared_heads", rows_prepared)]
-        if batch.is_decode:
-            variants.append(("row_ids_no_index", rows_no_index))
-        for name, fn in variants:
-            s = torch.cuda.Stream(device)
-            s.wait_stream(torch.cuda.current_stream(device))
-            with torch.cuda.stream(s):
-                fn()
-            torch.cuda.current_stream(device).wait_stream(s)
-            torch.cuda.synchronize(device)
-            g = torch.cuda.CUDAGraph()
-            calls = 300
-            with torch.cuda.graph(g):
-                for _ in range(calls):
-                    fn()
-            g.replay()
-            torch.cuda.synchronize(device)
-            runs = []
-            for _ in range(7):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                g.replay()
-                e1.record()
-                torch.cuda.synchronize(device)
-                runs.append(1e3 * e0.elapsed_time(e1) / calls)
-            us = statistics.median(runs)
-            res[f"{name}_us"] = us
-            del g
-        res["row_ids_per_s"] = batch.row_ids_per_call / (res["step_us"] / 1e6)
-        res["row_ids_per_s_one_launch"] = batch.row_ids_per_call / (res["step_one_launch_us"] / 1e6)
-        res["kernel_gbs"] = batch.algorithmic_bytes() / (res["row_ids_us"] / 1e6) / 1e9
-        res["kernel_frac_of_measured_hbm"] = res["kernel_gbs"] / peaks["hbm_gbs"]
-        bytes32 = batch.algorithmic_bytes() - 4 * L * T * H
-        res["i32_algorithmic_bytes"] = bytes32
-        res["i32_kernel_gbs"] = bytes32 / (res["row_ids_i32_us"] / 1e6) / 1e9
-        res["i32_kernel_frac_of_measured_hbm"] = res["i32_kernel_gbs"] / peaks["hbm_gbs"]
-        out.append(res)
-        print(json.dumps(res), file=sys.stderr, flush=True)
-    print(json.dumps({"all_configs": out, "method": "CUDA graph of 300 back-to-back calls, "
-                      "median of 7 replays; step = ple_build_token_index + ple_row_ids; "
-                      "step_one_launch = ple_row_ids without an index (cu_seqlens searched in "
-                      "the kernel for a prefill, req = t for a decode)"}))
+    clocks = ClockSampler("0")
+    clocks.start()
+    out = {}
+    if not args.only or "decode_b1_latency" in args.only:
+        out["decode_b1"] = decode_latency(ple, torch, device)
+    out["configs"] = all_configs(args, ple, torch, device, clocks, peaks)
+    clocks.stop()
+    print(json.dumps(out))
     return 0
 
 
-def embed_bench(args):
-    """The fused table gather on the large-prefill shape: a 256-wide bfloat16
-    table per layer with one row per head vocabulary entry (about 7.1 M rows,
-    29 GB over 8 layers), one JSON line with the gather's HBM rate."""
-    import torch
-
-    import layer_gram_embedding_gb300 as ple
-    from layer_gram_embedding_gb300 import build as lib_build
-
-    lib_build.build()
-    device = torch.device("cuda", 0)
-    b = wl.prefill_262144()
+def embed_entry(args, ple, torch, device, clocks, b, peaks):
+    """The fused table gather (ple_row_embed, requests found from cu_seqlens)
+    on one workload: a D-wide bfloat16 table per layer with one row per head
+    vocabulary entry; device time per call from a graph of 20 calls, median
+    of 7 replays."""
     if args.embed_layers < b.num_layers:
-        # fewer layers keep a profiling capture within a few GB of table
         k = max(1, args.embed_layers)
-        b = wl.replace(b, layer_multipliers=b.layer_multipliers[:k], vocab_sizes=b.vocab_sizes[:k],
-                       offsets=b.offsets[:k])
+        b = wl.replace(b, layer_multipliers=b.layer_multipliers[:k],
+                       vocab_sizes=b.vocab_sizes[:k], offsets=b.offsets[:k])
     T, B, L, H, N = b.num_tokens, b.num_requests, b.num_layers, b.num_heads, b.ngram_size
     D = args.embed_dim
     V = int(b.vocab_sizes.sum(axis=1).max())
@@ -823,37 +1003,46 @@ def embed_bench(args):
     table = torch.randn((L, V, D), dtype=torch.bfloat16, device=device, generator=gen)
     ids, ctx, cu = to_dev(b.ids), to_dev(b.ngram_context), to_dev(b.cu_seqlens)
     M, vocab, off = to_dev(b.layer_multipliers), to_dev(b.vocab_sizes), to_dev(b.offsets)
-    req, local = ple.ple_build_token_index(cu, B, T, False)
     out = torch.empty((L, T, D), dtype=torch.float32, device=device)
 
     def call():
-        ple.ple_row_embed(ids, req, local, ctx, M, vocab, off, N, b.heads_per_ngram,
-                          b.boundary_id, table, out=out)
+        ple.ple_row_embed(ids, None, None, ctx, M, vocab, off, N, b.heads_per_ngram,
+                          b.boundary_id, table, out=out, cu_seqlens=cu)
 
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize(device)
-    steps = max(3, min(args.steps, 50))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        call()
-    e1.record()
-    torch.cuda.synchronize(device)
-    ms = e0.elapsed_time(e1) / steps
-    gather = L * T * H * D * 2
-    written = L * T * D * 4
-    total = gather + written + T * 16 + B * (N - 1) * 8 + 8 * L * (N + 2 * H)
-    peaks, kind = measured_peaks()
-    gbs = total / (ms / 1e3) / 1e9
-    print(json.dumps({
-        "metric": "fused PLE table gather (hash + gather, row ids never written)",
-        "workload": f"{b.name}: T={T}, L={L}, H={H}, D={D}, V={V} rows per layer, bf16 table "
-                    f"{L * V * D * 2 / 1e9:.1f} GB, fp32 out",
-        "ms_per_call": ms, "embeddings_per_s": L * T / (ms / 1e3),
-        "algorithmic_bytes": total, "gather_bytes": gather, "out_bytes": written,
-        "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
-        "peak_kind": kind, "steps": steps, "launches_per_call": 1}))
+    key = "embed_" + b.name
+    clocks.mark(key, True)
+    us, _ = graph_us_per_call(torch, device, [call], 20)
+    clocks.mark(key, False)
+    nb = call_bytes(b, "cu", embed_dim=D)
+    gbs = nb / (us / 1e6) / 1e9
+    del table
+    torch.cuda.empty_cache()
+    return {"workload": b.name, "T": T, "L": L, "H": H, "D": D, "V": V,
+            "table_gb": L * V * D * 2 / 1e9, "us_per_call": us,
+            "embeddings_per_s": L * T / (us / 1e6), "algorithmic_bytes": nb,
+            "gather_bytes": L * T * H * D * 2, "out_bytes": L * T * D * 4,
+            "achieved_gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+            "launches_per_call": 1, "clocks": clocks.record(key),
+            "method": "CUDA graph of 20 calls, median of 7 replays"}
+
+
+def embed_bench(args):
+    """The fused table gather alone on one workload, one JSON line (for
+    profiling: --embed-layers 1 keeps the table to a few GB)."""
+    import torch
+
+    import layer_gram_embedding_gb300 as ple
+    from layer_gram_embedding_gb300 import build as lib_build
+
+    lib_build.build()
+    device = torch.device("cuda", 0)
+    peaks, _ = measured_peaks()
+    b = wl.prefill_262144_lowrep() if args.embed_workload == "lowrep" else wl.prefill_262144()
+    clocks = ClockSampler("0")
+    clocks.start()
+    res = embed_entry(args, ple, torch, device, clocks, b, peaks)
+    clocks.stop()
+    print(json.dumps(res))
     return 0
 
 
@@ -863,42 +1052,39 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--shard", action="store_true",
+                    help="split one batch by token range over the ranks (strong scaling)")
+    ap.add_argument("--min-timed-ms", type=float, default=250.0,
+                    help="repeat the K-step timed region until this much has been timed")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload figures")
+    ap.add_argument("--no-embed", action="store_true", help="skip the gather in the configs")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurements")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode B=1 latency")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-all-cores", action="store_true",
                     help="skip the all-cores oracle run beside the single-thread baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of single-thread oracle work for cpu_baseline")
+    ap.add_argument("--configs-only", action="store_true",
+                    help="only the per-workload figures (one JSON object)")
+    ap.add_argument("--only", nargs="+", default=None, metavar="KEY",
+                    help="with --configs-only: these entries only (e.g. mixed_8192, "
+                         "decode_b1, decode_b1_latency, row_embed_prefill_262144_lowrep)")
     ap.add_argument("--embed", action="store_true",
-                    help="time the fused table gather instead of the contract line")
+                    help="time only the fused table gather (one JSON line)")
+    ap.add_argument("--embed-workload", choices=["runs", "lowrep"], default="runs")
     ap.add_argument("--embed-dim", type=int, default=256)
     ap.add_argument("--embed-layers", type=int, default=8,
                     help="layers of the large prefill the gather runs (default all 8)")
-    ap.add_argument("--all-configs", action="store_true",
-                    help="time every workload (graph of 300 calls) instead of the contract line")
-    ap.add_argument("--only", nargs="+", default=None, metavar="WORKLOAD",
-                    help="with --all-configs: only these workloads (e.g. mixed_8192)")
-    ap.add_argument("--decode-only", action="store_true",
-                    help="only the decode B=1 latency (graph of 300 calls), one JSON object")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return reference_arm(args)
-    if args.all_configs:
-        return all_configs(args)
     if args.embed:
         return embed_bench(args)
-    if args.decode_only:
-        import torch
-
-        import layer_gram_embedding_gb300 as ple
-        from layer_gram_embedding_gb300 import build as lib_build
-
-        lib_build.build()
-        print(json.dumps({"decode_b1": decode_latency(ple, torch, torch.device("cuda", 0))}))
-        return 0
+    if args.configs_only:
+        return configs_only(args)
     return our_arm(args)
 
 

@@ -11,7 +11,8 @@
  *
  * Conventions shared by every entry point:
  *   - Every array argument is a DEVICE pointer (cudaMalloc'd or otherwise
- *     device-accessible) owned by the caller.  The library allocates nothing,
+ *     device-accessible) owned by the caller, except in ple_shard_plan,
+ *     which is host code on host arrays.  The library allocates nothing,
  *     keeps no per-call state, never reads device data on the host and never
  *     synchronises.  Inputs are read-only.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
@@ -294,6 +295,75 @@ ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int64_t num_to
                          void* stream);
 
 /*
+ * ple_shard_plan -- one rank's share of a batch split by token range (host
+ * code, host arrays; no CUDA call).
+ *
+ * Tokens are independent once each knows its window, and a request cut in
+ * the middle continues from a carried context row: the last ngram_size - 1
+ * ids before the cut (section "What", second observation: the window of a
+ * token near its request's start reaches into the carried context).  So a
+ * batch splits across ranks by token range with no exchange: rank k of
+ * world_size takes tokens [T*k/world, T*(k+1)/world) (integer division) and
+ * the requests that own them, hashes them as a batch of its own (inputs from
+ * ple_shard_inputs) and writes its own [L, token_end - token_begin, H] rows,
+ * which equal rows token_begin..token_end-1 of every layer of the whole
+ * batch.
+ *
+ *   cu_seqlens   [num_requests + 1] int32, HOST: the whole batch's
+ *                (non-decreasing, cu_seqlens[0] = 0, last = num_tokens;
+ *                checked here, since it is host data).  NULL for a decode
+ *                batch (one token per request): then the rank's requests
+ *                are its tokens.
+ *   num_requests B >= 1; num_tokens T >= 0 (T == B for a decode).
+ *   world_size   >= 1; rank in [0, world_size).
+ *   token_begin, token_end        out: the rank's tokens [begin, end).
+ *   request_begin, request_count  out: the requests owning them, a
+ *                contiguous range (request_count is 0 when the rank has no
+ *                token).  A request with no token that starts exactly at a
+ *                cut belongs to no rank; any other empty request between the
+ *                rank's first and last owner is included.
+ *
+ * Errors: PLE_ERR_NULL (an output pointer), PLE_ERR_SIZE (counts out of
+ * range, or cu_seqlens not a valid prefix sum of num_tokens).
+ */
+ple_status ple_shard_plan(const int32_t* cu_seqlens, int32_t num_requests, int64_t num_tokens,
+                          int32_t world_size, int32_t rank, int64_t* token_begin,
+                          int64_t* token_end, int32_t* request_begin, int32_t* request_count);
+
+/*
+ * ple_shard_inputs -- the per-rank inputs of ple_shard_plan's split, built on
+ * the device from the whole batch's device arrays (one launch, no host read).
+ *
+ *   input_ids, id_dtype   [num_tokens] the whole batch's ids, device.  The
+ *                         rank's ids are input_ids + token_begin (no copy).
+ *   cu_seqlens            [num_requests + 1] int32, device: the whole batch's.
+ *   ngram_context         [num_requests, ctx_len], dtype of the ids, device.
+ *   num_requests, num_tokens, ctx_len (= ngram_size - 1, 1..15): the whole
+ *                         batch's.
+ *   token_begin, token_end, request_begin, request_count: from
+ *                         ple_shard_plan (request_count >= 1).
+ *   shard_cu_seqlens      [request_count + 1] int32 out, device: the rank's
+ *                         cu_seqlens, cu_seqlens[request_begin + j] -
+ *                         token_begin clamped to [0, token_end - token_begin].
+ *   shard_context         [request_count, ctx_len] out, device, dtype of the
+ *                         ids: request request_begin + j's context row for
+ *                         the rank's call -- for the first request, cut at
+ *                         token_begin, the last ctx_len ids of (its context
+ *                         row, its tokens before token_begin); for the others
+ *                         their own context row.
+ *
+ * Device data outside these rules (malformed cu_seqlens) gives unspecified
+ * outputs but never an out-of-bounds access: every index is clamped.
+ * Errors: PLE_ERR_NULL, PLE_ERR_SIZE, PLE_ERR_DTYPE, PLE_ERR_ALIGN,
+ * PLE_ERR_CUDA.  One kernel launch.
+ */
+ple_status ple_shard_inputs(const void* input_ids, int32_t id_dtype, const int32_t* cu_seqlens,
+                            const void* ngram_context, int32_t num_requests, int64_t num_tokens,
+                            int32_t ctx_len, int64_t token_begin, int64_t token_end,
+                            int32_t request_begin, int32_t request_count,
+                            int32_t* shard_cu_seqlens, void* shard_context, void* stream);
+
+/*
  * ple_validate_index -- diagnostic: check the index preconditions on the
  * device.
  *
@@ -344,6 +414,23 @@ ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
  * A library tuning constant with no counterpart on the page; the row ids do
  * not depend on it. */
 int64_t ple_small_batch_max_rows(void);
+
+/*
+ * ple_set_programmatic_launch -- process-wide switch for programmatic
+ * dependent launch (on by default); returns the previous setting (1 or 0).
+ *
+ * Launch behaviour only, with no counterpart on the page: the row ids do not
+ * depend on it.  When on, every kernel of this library is launched with
+ * programmatic stream serialization and waits for the preceding grid in the
+ * stream to complete before its first global memory access; so the launch of
+ * one call overlaps the kernel before it (back-to-back calls, or the token
+ * index build, which lets its dependent start at once, followed by the
+ * row-id hash), and no memory is read early.
+ * Off: every launch is an ordinary stream-ordered launch, so each call's
+ * device time stands alone (for example, to time one call without overlap).
+ * Takes effect for launches issued after it returns; safe from any thread.
+ */
+int32_t ple_set_programmatic_launch(int32_t enabled);
 
 /* Static, NUL-terminated description of a status code ("unknown status"
  * for values outside ple_status). */

@@ -55,6 +55,10 @@ SIGNATURES = {
     "ple_status_string": (ctypes.c_char_p, [_I32]),
     "ple_last_cuda_error": (_I32, []),
     "ple_small_batch_max_rows": (_I64, []),
+    "ple_set_programmatic_launch": (_I32, [_I32]),
+    "ple_shard_plan": (_I32, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P]),
+    "ple_shard_inputs": (_I32, [_P, _I32, _P, _P, _I32, _I64, _I32, _I64, _I64, _I32, _I32, _P,
+                                _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -99,6 +103,14 @@ def small_batch_max_rows() -> int:
     """Batches of at most this many row ids (T * H * L) run the small-batch
     kernel; the row ids do not depend on which kernel runs."""
     return int(lib().ple_small_batch_max_rows())
+
+
+def set_programmatic_launch(enabled: bool) -> bool:
+    """Turn programmatic dependent launch of every library kernel on or off
+    (process-wide; on by default); returns the previous setting.  Off, each
+    call is an ordinary stream-ordered launch, so one call's device time
+    stands alone; the row ids are the same either way."""
+    return bool(lib().ple_set_programmatic_launch(1 if enabled else 0))
 
 
 def _check(status: int, where: str):
@@ -168,6 +180,72 @@ def ple_build_token_index(cu_seqlens, num_requests: int, num_tokens: int, is_dec
                                          _ptr(req), _ptr(local), _stream_handle(stream, dev))
     _check(st, where)
     return req, local
+
+
+def ple_shard_plan(cu_seqlens, num_requests: int, num_tokens: int, world_size: int,
+                   rank: int):
+    """(token_begin, token_end, request_begin, request_count) of one rank's
+    share of a batch split by token range -- host code on a host int32
+    cu_seqlens [num_requests + 1] (numpy array or CPU tensor), or None for a
+    decode batch.  Needs no GPU."""
+    where = "ple_shard_plan"
+    cu_p = ctypes.c_void_p(0)
+    keep = None
+    if cu_seqlens is not None:
+        keep = torch.as_tensor(cu_seqlens)
+        if keep.device.type != "cpu" or keep.dtype != torch.int32:
+            raise ValueError(f"{where}: cu_seqlens must be a host int32 array")
+        keep = keep.contiguous()
+        if keep.numel() != int(num_requests) + 1:
+            raise ValueError(f"{where}: cu_seqlens must have num_requests + 1 elements")
+        cu_p = ctypes.c_void_p(keep.data_ptr())
+    tb, te = ctypes.c_int64(), ctypes.c_int64()
+    rb, rc = ctypes.c_int32(), ctypes.c_int32()
+    st = lib().ple_shard_plan(cu_p, int(num_requests), int(num_tokens), int(world_size),
+                              int(rank), ctypes.byref(tb), ctypes.byref(te), ctypes.byref(rb),
+                              ctypes.byref(rc))
+    _check(st, where)
+    del keep
+    return tb.value, te.value, rb.value, rc.value
+
+
+def ple_shard_inputs(input_ids: torch.Tensor, cu_seqlens: torch.Tensor,
+                     ngram_context: torch.Tensor, plan, shard_cu_seqlens=None,
+                     shard_context=None, stream=None):
+    """One rank's (ids, cu_seqlens, ngram_context) for its plan from
+    ple_shard_plan, built on the device from the whole batch's device
+    tensors (one launch).  The ids are a view of input_ids; the other two are
+    written into shard_cu_seqlens [request_count + 1] int32 and shard_context
+    [request_count, ngram_size - 1] (allocated when None)."""
+    where = "ple_shard_inputs"
+    tb, te, rb, rc = (int(x) for x in plan)
+    dev = _one_cuda_device([input_ids, cu_seqlens, ngram_context], where)
+    if input_ids.dtype not in (torch.int32, torch.int64) or ngram_context.dtype != input_ids.dtype:
+        raise ValueError(f"{where}: ids and context must be int32 or int64, same dtype")
+    _need(cu_seqlens, torch.int32, "cu_seqlens", where)
+    if ngram_context.dim() != 2:
+        raise ValueError(f"{where}: ngram_context must be [B, ngram_size - 1]")
+    B, C = ngram_context.shape
+    if shard_cu_seqlens is None:
+        shard_cu_seqlens = torch.empty(max(rc, 0) + 1, dtype=torch.int32, device=dev)
+    if shard_context is None:
+        shard_context = torch.empty((max(rc, 0), C), dtype=input_ids.dtype, device=dev)
+    _one_cuda_device([input_ids, shard_cu_seqlens, shard_context], where)
+    if shard_cu_seqlens.numel() != rc + 1 or tuple(shard_context.shape) != (rc, C):
+        raise ValueError(f"{where}: outputs must be [request_count + 1] and [request_count, C]")
+    for name, t in (("input_ids", input_ids), ("cu_seqlens", cu_seqlens),
+                    ("ngram_context", ngram_context), ("shard_cu_seqlens", shard_cu_seqlens),
+                    ("shard_context", shard_context)):
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+    dt = PLE_I32 if input_ids.dtype == torch.int32 else PLE_I64
+    with torch.cuda.device(dev):
+        st = lib().ple_shard_inputs(_ptr(input_ids), dt, _ptr(cu_seqlens), _ptr(ngram_context),
+                                    int(B), int(input_ids.numel()), int(C), tb, te, rb, rc,
+                                    _ptr(shard_cu_seqlens), _ptr(shard_context),
+                                    _stream_handle(stream, dev))
+    _check(st, where)
+    return input_ids[tb:te], shard_cu_seqlens, shard_context
 
 
 def ple_row_ids(input_ids: torch.Tensor, req: torch.Tensor | None, local: torch.Tensor | None,

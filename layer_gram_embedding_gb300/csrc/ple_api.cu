@@ -1,11 +1,14 @@
 // C ABI of the PLE n-gram row-id hash library (declared in include/ple.h).
 //
 // Every entry point validates its scalar arguments and pointer values on the
-// host, then enqueues exactly one kernel on the caller's stream.  Nothing is
-// allocated, nothing is read back, nothing is cached except per-device facts
-// (SM count, shared-memory limit) looked up once.
+// host, then enqueues exactly one kernel on the caller's stream and reports
+// that launch's own status; the caller's pending CUDA error state is left as
+// it was.  Nothing is allocated, nothing is read back, nothing is cached
+// except per-device facts (SM count, shared-memory limit) looked up once and
+// the process-wide programmatic-launch switch.
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ple.h"
@@ -18,7 +21,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_facts_mu;
 bool g_facts_ok[kMaxDevices];
 DeviceFacts g_facts[kMaxDevices];
+std::atomic<int> g_programmatic{1};
 }  // namespace
+
+bool programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
 
 cudaError_t device_facts(DeviceFacts* out) {
     int dev = 0;
@@ -64,7 +70,6 @@ extern "C" ple_status ple_build_token_index(const int32_t* cu_seqlens, int32_t n
     if (!req || !local || (!is_decode && !cu_seqlens)) return PLE_ERR_NULL;
     if (!aligned(req, 4) || !aligned(local, 4) || (!is_decode && !aligned(cu_seqlens, 4)))
         return PLE_ERR_ALIGN;
-    (void)cudaGetLastError();  // start from a clean per-thread error state
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -167,7 +172,6 @@ ple_status row_ids_impl(const void* input_ids, int32_t id_dtype, int64_t num_tok
     const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
     if (!aligned(out, out_bytes) || !aligned(next_context, id_bytes)) return PLE_ERR_ALIGN;
 
-    (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -236,7 +240,6 @@ extern "C" ple_status ple_prepare_heads(const int64_t* vocab_sizes, const int64_
     if (!vocab_sizes || !offsets || !heads) return PLE_ERR_NULL;
     if (!aligned(vocab_sizes, 8) || !aligned(offsets, 8) || !aligned(heads, 16))
         return PLE_ERR_ALIGN;
-    (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -272,7 +275,6 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     if (!out || (table_rows > 0 && !table)) return PLE_ERR_NULL;
     if (!aligned(table, 16) || !aligned(out, 16)) return PLE_ERR_ALIGN;
 
-    (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -289,6 +291,84 @@ extern "C" ple_status ple_row_embed(const void* input_ids, int32_t id_dtype, int
     return PLE_OK;
 }
 
+extern "C" ple_status ple_shard_plan(const int32_t* cu_seqlens, int32_t num_requests,
+                                     int64_t num_tokens, int32_t world_size, int32_t rank,
+                                     int64_t* token_begin, int64_t* token_end,
+                                     int32_t* request_begin, int32_t* request_count) {
+    if (!token_begin || !token_end || !request_begin || !request_count) return PLE_ERR_NULL;
+    if (num_tokens < 0 || num_tokens > INT32_MAX || num_requests < 1 || world_size < 1 ||
+        rank < 0 || rank >= world_size)
+        return PLE_ERR_SIZE;
+    const int64_t T = num_tokens;
+    const int64_t a = T * rank / world_size;
+    const int64_t b = T * (rank + 1) / world_size;
+    if (!cu_seqlens) {
+        // a decode batch: token t is request t
+        if ((int64_t)num_requests != T) return PLE_ERR_SIZE;
+        *token_begin = a;
+        *token_end = b;
+        *request_begin = (int32_t)a;
+        *request_count = (int32_t)(b - a);
+        return PLE_OK;
+    }
+    // host data: check it is a prefix sum of T
+    if (cu_seqlens[0] != 0 || (int64_t)cu_seqlens[num_requests] != T) return PLE_ERR_SIZE;
+    for (int32_t r = 0; r < num_requests; ++r)
+        if (cu_seqlens[r + 1] < cu_seqlens[r]) return PLE_ERR_SIZE;
+    *token_begin = a;
+    *token_end = b;
+    if (a == b) {
+        *request_begin = 0;
+        *request_count = 0;
+        return PLE_OK;
+    }
+    // the owner of token t: the last r with cu_seqlens[r] <= t
+    auto owner = [&](int64_t t) {
+        int32_t lo = 0, hi = num_requests - 1;
+        while (lo < hi) {
+            const int32_t mid = lo + (hi - lo + 1) / 2;
+            if ((int64_t)cu_seqlens[mid] <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    };
+    const int32_t r0 = owner(a);
+    const int32_t r1 = owner(b - 1);
+    *request_begin = r0;
+    *request_count = r1 - r0 + 1;
+    return PLE_OK;
+}
+
+extern "C" ple_status ple_shard_inputs(const void* input_ids, int32_t id_dtype,
+                                       const int32_t* cu_seqlens, const void* ngram_context,
+                                       int32_t num_requests, int64_t num_tokens, int32_t ctx_len,
+                                       int64_t token_begin, int64_t token_end,
+                                       int32_t request_begin, int32_t request_count,
+                                       int32_t* shard_cu_seqlens, void* shard_context,
+                                       void* stream) {
+    if (num_requests < 1 || num_tokens < 1 || num_tokens > INT32_MAX || ctx_len < 1 ||
+        ctx_len >= PLE_MAX_NGRAM || token_begin < 0 || token_end <= token_begin ||
+        token_end > num_tokens || request_begin < 0 || request_count < 1 ||
+        (int64_t)request_begin + request_count > num_requests)
+        return PLE_ERR_SIZE;
+    if (!input_ids || !cu_seqlens || !ngram_context || !shard_cu_seqlens || !shard_context)
+        return PLE_ERR_NULL;
+    if (id_dtype != PLE_I32 && id_dtype != PLE_I64) return PLE_ERR_DTYPE;
+    const int id_bytes = id_dtype == PLE_I32 ? 4 : 8;
+    if (!aligned(input_ids, id_bytes) || !aligned(ngram_context, id_bytes) ||
+        !aligned(shard_context, id_bytes) || !aligned(cu_seqlens, 4) ||
+        !aligned(shard_cu_seqlens, 4))
+        return PLE_ERR_ALIGN;
+    cudaError_t e = ple::launch_shard_inputs(
+        input_ids, id_bytes, cu_seqlens, ngram_context, num_requests, num_tokens, ctx_len,
+        token_begin, token_end, request_begin, request_count, shard_cu_seqlens, shard_context,
+        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_failure(e);
+    return PLE_OK;
+}
+
 extern "C" ple_status ple_validate_index(const int32_t* cu_seqlens, int32_t num_requests,
                                          int64_t num_tokens, int32_t is_decode,
                                          const int32_t* req, const int32_t* local,
@@ -301,7 +381,6 @@ extern "C" ple_status ple_validate_index(const int32_t* cu_seqlens, int32_t num_
     if (!aligned(req, 4) || !aligned(local, 4) || !aligned(first_bad, 8) ||
         (!is_decode && !aligned(cu_seqlens, 4)))
         return PLE_ERR_ALIGN;
-    (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -318,7 +397,6 @@ extern "C" ple_status ple_selftest_floor_mod(const int64_t* x, const int64_t* v,
     if (!x || !v || !out_fast || !out_ref) return PLE_ERR_NULL;
     if (!aligned(x, 8) || !aligned(v, 8) || !aligned(out_fast, 8) || !aligned(out_ref, 8))
         return PLE_ERR_ALIGN;
-    (void)cudaGetLastError();
     ple::DeviceFacts dev;
     cudaError_t e = ple::device_facts(&dev);
     if (e != cudaSuccess) return cuda_failure(e);
@@ -346,3 +424,7 @@ extern "C" const char* ple_status_string(int32_t status) {
 extern "C" int32_t ple_last_cuda_error(void) { return g_last_cuda_error; }
 
 extern "C" int64_t ple_small_batch_max_rows(void) { return ple::kSmallMaxRows; }
+
+extern "C" int32_t ple_set_programmatic_launch(int32_t enabled) {
+    return ple::g_programmatic.exchange(enabled ? 1 : 0) != 0 ? 1 : 0;
+}

@@ -179,19 +179,8 @@ cudaError_t launch_row_embed(const RowIdsParams& p, const EmbedArgs& e, int id_b
                                                (int)cfg.smem_bytes);
         if (err != cudaSuccess) return err;
     }
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = cfg.grid;
-    lc.blockDim = cfg.block;
-    lc.dynamicSmemBytes = cfg.smem_bytes;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&lc, fn, p, e);
-    if (err != cudaSuccess) return err;
-    return cudaGetLastError();
+    return launch_kernel(fn, cfg.grid, cfg.block, cfg.smem_bytes, stream, programmatic_launch(),
+                         p, e);
 }
 
 }  // namespace ple

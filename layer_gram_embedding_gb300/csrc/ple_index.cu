@@ -95,6 +95,43 @@ token_index_prefill_kernel(const int32_t* __restrict__ cu, int32_t B, int64_t T,
     }
 }
 
+// One rank's inputs of a batch split by token range (ple_shard_inputs): its
+// cu_seqlens, rebased to its first token, and each of its requests' context
+// row -- the first request's continued across the cut from the ids before
+// it.  Thread j handles shard request j (and shard cu_seqlens entry j); every
+// device-supplied index is clamped into its array.
+template <typename IdT>
+__global__ void __launch_bounds__(kIndexThreads)
+shard_inputs_kernel(const IdT* __restrict__ ids, const int32_t* __restrict__ cu,
+                    const IdT* __restrict__ ctx, int32_t B, int64_t T, int32_t C,
+                    int64_t tok_begin, int64_t tok_end, int32_t req_begin, int32_t req_count,
+                    int32_t* __restrict__ shard_cu, IdT* __restrict__ shard_ctx) {
+    cudaTriggerProgrammaticLaunchCompletion();
+    cudaGridDependencySynchronize();
+    const int64_t span = tok_end - tok_begin;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= req_count;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = req_begin + j;  // <= B: checked on the host
+        const int64_t start = __ldg(cu + r);
+        shard_cu[j] = (int32_t)min(max(start - tok_begin, (int64_t)0), span);
+        if (j == req_count) break;
+        // tokens of request r before the cut, k: the carried row is the last
+        // C ids of (context row r, those k tokens)
+        const int64_t k = min(max(tok_begin - start, (int64_t)0), T);
+        for (int c = 0; c < C; ++c) {
+            const int64_t i = k + c;  // position in (context row, tokens)
+            IdT v;
+            if (i < C) {
+                v = ctx[r * C + i];
+            } else {
+                const int64_t t = min(max(start + i - C, (int64_t)0), T - 1);
+                v = ids[t];
+            }
+            shard_ctx[j * C + c] = v;
+        }
+    }
+}
+
 // First token whose (req, local) differs from the index cu_seqlens (or the
 // decode rule) defines; *first_bad is lowered to it with an atomic min.
 __global__ void __launch_bounds__(kIndexThreads)
@@ -154,6 +191,7 @@ selftest_floor_mod_kernel(const int64_t* __restrict__ x, const int64_t* __restri
 __global__ void __launch_bounds__(kIndexThreads)
 prepare_heads_kernel(const int64_t* __restrict__ vocab, const int64_t* __restrict__ offsets,
                      int64_t n, void* __restrict__ heads) {
+    cudaTriggerProgrammaticLaunchCompletion();
     cudaGridDependencySynchronize();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride)
@@ -170,20 +208,17 @@ unsigned grid_for(int64_t n, const DeviceFacts& dev) {
 
 }  // namespace
 
-// Launch with programmatic stream serialization (see the kernels).
-template <typename... Args>
-cudaError_t launch_pdl(void (*fn)(Args...), unsigned grid, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(grid);
-    lc.blockDim = dim3(kIndexThreads);
-    lc.dynamicSmemBytes = 0;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, fn, args...);
+// Launch with programmatic stream serialization (see the kernels) unless it
+// is turned off; the diagnostics launch plainly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), unsigned grid, cudaStream_t stream, Args... args) {
+    return launch_kernel(fn, dim3(grid), dim3(kIndexThreads), 0, stream, programmatic_launch(),
+                         args...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*fn)(KArgs...), unsigned grid, cudaStream_t stream, Args... args) {
+    return launch_kernel(fn, dim3(grid), dim3(kIndexThreads), 0, stream, false, args...);
 }
 
 cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
@@ -203,32 +238,42 @@ cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t 
         e = staged ? launch_pdl(token_index_prefill_kernel<false, true>, g, stream, cu, B, T, req, local)
                    : launch_pdl(token_index_prefill_kernel<false, false>, g, stream, cu, B, T, req, local);
     }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return e;
+}
+
+cudaError_t launch_shard_inputs(const void* ids, int id_bytes, const int32_t* cu,
+                                const void* ctx, int32_t B, int64_t T, int32_t C,
+                                int64_t tok_begin, int64_t tok_end, int32_t req_begin,
+                                int32_t req_count, int32_t* shard_cu, void* shard_ctx,
+                                cudaStream_t stream) {
+    const unsigned g = (unsigned)((req_count + kIndexThreads) / kIndexThreads);
+    if (id_bytes == 4)
+        return launch_pdl(shard_inputs_kernel<int32_t>, g, stream,
+                          static_cast<const int32_t*>(ids), cu, static_cast<const int32_t*>(ctx),
+                          B, T, C, tok_begin, tok_end, req_begin, req_count, shard_cu,
+                          static_cast<int32_t*>(shard_ctx));
+    return launch_pdl(shard_inputs_kernel<int64_t>, g, stream, static_cast<const int64_t*>(ids),
+                      cu, static_cast<const int64_t*>(ctx), B, T, C, tok_begin, tok_end, req_begin,
+                      req_count, shard_cu, static_cast<int64_t*>(shard_ctx));
 }
 
 cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                   const int32_t* req, const int32_t* local, int64_t* first_bad,
                                   const DeviceFacts& dev, cudaStream_t stream) {
-    validate_index_kernel<<<grid_for(T, dev), kIndexThreads, 0, stream>>>(
-        cu, B, T, is_decode, req, local, reinterpret_cast<unsigned long long*>(first_bad));
-    return cudaGetLastError();
+    return launch_plain(validate_index_kernel, grid_for(T, dev), stream, cu, B, T, is_decode, req,
+                        local, reinterpret_cast<unsigned long long*>(first_bad));
 }
 
 cudaError_t launch_prepare_heads(const int64_t* vocab, const int64_t* offsets, int64_t n,
                                  void* heads, const DeviceFacts& dev, cudaStream_t stream) {
-    cudaError_t e = launch_pdl(prepare_heads_kernel, grid_for(n, dev), stream, vocab, offsets, n,
-                               heads);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_pdl(prepare_heads_kernel, grid_for(n, dev), stream, vocab, offsets, n, heads);
 }
 
 cudaError_t launch_selftest_floor_mod(const int64_t* x, const int64_t* v, int64_t n,
                                       int64_t* out_fast, int64_t* out_ref, const DeviceFacts& dev,
                                       cudaStream_t stream) {
-    selftest_floor_mod_kernel<<<grid_for(n, dev), kIndexThreads, 0, stream>>>(x, v, n, out_fast,
-                                                                              out_ref);
-    return cudaGetLastError();
+    return launch_plain(selftest_floor_mod_kernel, grid_for(n, dev), stream, x, v, n, out_fast,
+                        out_ref);
 }
 
 }  // namespace ple

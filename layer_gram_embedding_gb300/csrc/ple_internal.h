@@ -103,6 +103,32 @@ struct EmbedArgs {
     float* out;
 };
 
+// Whether kernels are launched with programmatic stream serialization
+// (process-wide, on unless turned off by ple_set_programmatic_launch).
+bool programmatic_launch();
+
+// Launches fn on stream and returns the launch's own status (the caller's
+// pending CUDA error state is neither read nor cleared).  With programmatic
+// stream serialization the launch may begin while the kernel before it in
+// the stream drains: every kernel of this library waits for its predecessor
+// grid before its first global memory access, so nothing is read early, and
+// the launch overhead of back-to-back calls overlaps the kernel before.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool programmatic, Args... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = programmatic ? attr : nullptr;
+    lc.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, fn, args...);
+}
+
 struct RowIdsLaunch {
     dim3 grid;
     dim3 block;
@@ -141,6 +167,12 @@ cudaError_t launch_row_embed(const RowIdsParams& p, const EmbedArgs& e, int id_b
 cudaError_t launch_token_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                int32_t* req, int32_t* local, const DeviceFacts& dev,
                                cudaStream_t stream);
+
+cudaError_t launch_shard_inputs(const void* ids, int id_bytes, const int32_t* cu,
+                                const void* ctx, int32_t B, int64_t T, int32_t C,
+                                int64_t tok_begin, int64_t tok_end, int32_t req_begin,
+                                int32_t req_count, int32_t* shard_cu, void* shard_ctx,
+                                cudaStream_t stream);
 
 cudaError_t launch_validate_index(const int32_t* cu, int32_t B, int64_t T, int32_t is_decode,
                                   const int32_t* req, const int32_t* local, int64_t* first_bad,

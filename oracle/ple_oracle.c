@@ -21,7 +21,7 @@
  *     the divisor's sign); the context holds ngram_size-1 ids and each n-gram
  *     order owns heads_per_ngram heads.
  *
- * Readings taken where the page is silent (each is listed in the design doc):
+ * Readings taken where the page is silent (the readings below):
  *   - an invalid shift hashes the boundary id in place of the window value
  *     (reading "A"); reading "B" (an invalid shift contributes nothing to the
  *     XOR) is kept behind the `invalid_as_zero` flag for comparison only;

@@ -51,6 +51,15 @@ def test_status_strings(lib):
     assert lib.ple_last_cuda_error() == 0
 
 
+def test_programmatic_launch_switch(lib):
+    # host-side only: the switch is process-wide and returns the previous value
+    assert ple.set_programmatic_launch(False) is True
+    assert ple.set_programmatic_launch(False) is False
+    assert ple.set_programmatic_launch(True) is False
+    assert lib.ple_set_programmatic_launch(7) == 1
+    assert lib.ple_set_programmatic_launch(1) == 1
+
+
 # fake, never dereferenced device addresses: every call below fails a host
 # check before the library touches CUDA
 A = 0x10000

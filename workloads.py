@@ -233,6 +233,21 @@ def prefill_262144(replay: int = 0, ids_dtype=np.int64, context_all_boundary: bo
     return batch.with_ids_dtype(ids_dtype) if ids_dtype != np.int64 else batch
 
 
+def prefill_262144_lowrep(replay: int = 0) -> Batch:
+    """The large prefill's shape (T=262144 in 4 requests, ngram_size 4,
+    12 heads, 8 layers) with the ragged and mixed batches' boundary density:
+    2% isolated boundary ids at uniform positions (no runs), so that windows,
+    and the row ids they hash to, rarely repeat -- the input for measuring
+    the table gather's random-row rate without repeated rows served from L2."""
+    rng = np.random.default_rng(5 * 1000 + replay)
+    N, hpn, L, B, T = 4, 4, 8, 4, 262144
+    M, vocab, off = _params(rng, L, N, hpn, 2 ** 17, 2 ** 20)
+    cu = cu_from_lengths(random_split(rng, T, B))
+    ids = uniform_ids(rng, T, 0.02)
+    ctx = uniform_ids(rng, B * (N - 1), 0.02).reshape(B, N - 1)
+    return Batch("prefill_262144_lowrep", ids, ctx, cu, False, M, vocab, off, N, hpn)
+
+
 def all_workloads(replay: int = 0):
     """Every configuration the hash is checked on, small first."""
     out = [prefill_512(replay)]
