@@ -554,6 +554,16 @@ def our_arm(args):
         if not args.shard:
             step_with_index(i)
     torch.cuda.synchronize(device)
+    # beyond the W warm-up steps, untimed steps for --prewarm-ms of device
+    # time, so that an idle GPU's clocks have ramped before the first timed
+    # region (a run timed straight after start-up read twice the step time)
+    t_end = time.perf_counter() + args.prewarm_ms / 1e3
+    i = args.warmup
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            main_step(i)
+            i += 1
+        torch.cuda.synchronize(device)
 
     # ---- the timed regions: K steps back to back each, repeated
     clocks.mark("headline", True)
@@ -1054,6 +1064,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--shard", action="store_true",
                     help="split one batch by token range over the ranks (strong scaling)")
+    ap.add_argument("--prewarm-ms", type=float, default=200.0,
+                    help="untimed steps for this long after the warm-up steps (clock ramp)")
     ap.add_argument("--min-timed-ms", type=float, default=250.0,
                     help="repeat the K-step timed region until this much has been timed")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload figures")

@@ -29,18 +29,24 @@ constexpr int kMaxWarps = PLE_MAX_WARPS;
 constexpr int kFixedMinBlocks = PLE_FIXED_MIN_BLOCKS;
 // Launch-shape target: thread blocks per SM the layer grouping aims for --
 // 32 for int64 row ids (write-bound: smaller layer groups keep more
-// independent stores in flight), 16 for int32 row ids (bound by the
-// integer-multiply pipe: larger groups share each token's window) and for
-// the fused gather.  Measured on GB300: the large prefill's one-launch step
-// 30.4 -> 30.0 us and the mixed batch's 18.3 -> 17.3 us at 32, while the
-// large prefill's int32 output lost 2%.
+// independent stores in flight), 8 for int32 row ids (bound by instruction
+// issue: larger groups share each token's window and cost fewer, longer
+// blocks), 16 for the fused gather.  Measured on GB300: the large prefill's
+// one-launch step 30.4 -> 30.0 us and the mixed batch's 18.3 -> 17.3 us at 32
+// (against 16); int32 row ids of the large prefill 22.6 -> 21.9 us and of the
+// mixed batch 13.6 -> 13.3 us at 8 (against 16; 5 was better for the large
+// prefill, 21.6 us, but worse for the mixed batch, 14.6 us).
 #ifndef PLE_BLOCKS_PER_SM
-#define PLE_BLOCKS_PER_SM 16
+#define PLE_BLOCKS_PER_SM 8
 #endif
 #ifndef PLE_BLOCKS_PER_SM_I64
 #define PLE_BLOCKS_PER_SM_I64 32
 #endif
+#ifndef PLE_BLOCKS_PER_SM_EMBED
+#define PLE_BLOCKS_PER_SM_EMBED 16
+#endif
 constexpr int kTargetBlocksPerSm = PLE_BLOCKS_PER_SM;
+constexpr int kTargetBlocksPerSmEmbed = PLE_BLOCKS_PER_SM_EMBED;
 constexpr int kTargetBlocksPerSmI64 = PLE_BLOCKS_PER_SM_I64;
 // A grid with fewer blocks than this many per SM (times the SM count) takes
 // fewer warps per block, so that its warps spread over more SMs (0: never).

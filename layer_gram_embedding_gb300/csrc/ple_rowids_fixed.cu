@@ -305,7 +305,9 @@ row_ids_fixed_kernel(const RowIdsParams p) {
 #pragma unroll
     for (int j = 0; j < KU; ++j) {
         const int cj = (32 * j) % KU;
-        const bool carry = r0 + cj >= KU;
+        // cj == 0 (KU divides 32) folds the carry away: the offsets are then
+        // affine in j and need no registers of their own
+        const bool carry = cj != 0 && r0 + cj >= KU;
         const int col = r0 + cj - (carry ? KU : 0);
         stok[j] = q0 + (32 * j) / KU + (carry ? 1 : 0);
         if constexpr (kQuadStage)

@@ -120,8 +120,9 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     // so the last wave is short even when T alone gives few tiles; constants
     // stay within their shared-memory budget
     int64_t blocks_x = (tiles + warps - 1) / warps;
-    const int per_sm = !runtime_layout && p.out_bytes == 8 ? kTargetBlocksPerSmI64
-                                                           : kTargetBlocksPerSm;
+    const int per_sm = runtime_layout       ? kTargetBlocksPerSmEmbed
+                       : p.out_bytes == 8 ? kTargetBlocksPerSmI64
+                                          : kTargetBlocksPerSm;
     const int64_t target = per_sm * (int64_t)dev.sm_count;
     int64_t groups = (target + blocks_x - 1) / blocks_x;
     if (groups < 1) groups = 1;
