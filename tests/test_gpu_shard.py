@@ -113,3 +113,69 @@ def test_malformed_device_cu_seqlens_stays_in_bounds():
         assert (ctx_buf[0] == -7).all() and (ctx_buf[-1] == -7).all()
         s_cu = cu_buf[1:rc + 2].cpu().numpy()
         assert ((s_cu >= 0) & (s_cu <= te - tb)).all()
+
+
+def test_shard_step_in_a_cuda_graph_with_fresh_inputs():
+    """ple_shard_inputs + the one-launch row-id call captured once, replayed
+    three times with fresh ids and context copied into the captured inputs:
+    each replay equals the oracle's rows of that batch's share."""
+    base = wl.prefill_262144()
+    world, rank = 3, 1
+    plan = ple.ple_shard_plan(base.cu_seqlens, base.num_requests, base.num_tokens, world, rank)
+    tb, te, rb, rc = plan
+    ids = dev(base.ids)
+    ctx = dev(base.ngram_context)
+    cu = dev(base.cu_seqlens)
+    M, vocab, off = (dev(base.layer_multipliers), dev(base.vocab_sizes), dev(base.offsets))
+    s_cu = torch.empty(rc + 1, dtype=torch.int32, device=DEV)
+    s_ctx = torch.empty((rc, base.ngram_size - 1), dtype=torch.int64, device=DEV)
+    out = torch.empty((base.num_layers, te - tb, base.num_heads), dtype=torch.int64, device=DEV)
+
+    def step():
+        s_ids, _, _ = ple.ple_shard_inputs(ids, cu, ctx, plan, shard_cu_seqlens=s_cu,
+                                           shard_context=s_ctx)
+        ple.ple_row_ids(s_ids, None, None, s_ctx, M, vocab, off, base.ngram_size,
+                        base.heads_per_ngram, base.boundary_id, out=out, cu_seqlens=s_cu)
+
+    s = torch.cuda.Stream(DEV)
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream(DEV).wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for replay in range(1, 4):
+        fresh = wl.prefill_262144(replay=replay)
+        # the same request layout (the plan is fixed at capture): fresh ids and context
+        ids_np = fresh.ids.copy()
+        ids_np[base.cu_seqlens[:-1]] = base.boundary_id
+        ids.copy_(torch.from_numpy(ids_np))
+        ctx.copy_(torch.from_numpy(fresh.ngram_context))
+        g.replay()
+        torch.cuda.synchronize()
+        b = wl.replace(base, ids=ids_np, ngram_context=fresh.ngram_context)
+        rows, _, _ = whole_rows(b)
+        assert np.array_equal(out.cpu().numpy(), rows[:, tb:te, :]), replay
+
+
+def test_calls_without_programmatic_launch_give_the_same_rows():
+    """ple_set_programmatic_launch(False) changes how kernels are launched,
+    not what they compute."""
+    batch = wl.ragged_16()
+    rows, _, _ = whole_rows(batch)
+    args = (dev(batch.ids), None, None, dev(batch.ngram_context), dev(batch.layer_multipliers),
+            dev(batch.vocab_sizes), dev(batch.offsets), batch.ngram_size, batch.heads_per_ngram,
+            batch.boundary_id)
+    prev = ple.set_programmatic_launch(False)
+    try:
+        got = [ple.ple_row_ids(*args, cu_seqlens=dev(batch.cu_seqlens)) for _ in range(3)]
+        req, local = ple.ple_build_token_index(dev(batch.cu_seqlens), batch.num_requests,
+                                               batch.num_tokens, False)
+        got.append(ple.ple_row_ids(dev(batch.ids), req, local, *args[3:]))
+    finally:
+        ple.set_programmatic_launch(prev)
+    torch.cuda.synchronize()
+    for g in got:
+        assert np.array_equal(g.cpu().numpy(), rows)
