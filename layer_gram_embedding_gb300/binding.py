@@ -226,6 +226,10 @@ def ple_shard_inputs(input_ids: torch.Tensor, cu_seqlens: torch.Tensor,
     if ngram_context.dim() != 2:
         raise ValueError(f"{where}: ngram_context must be [B, ngram_size - 1]")
     B, C = ngram_context.shape
+    if cu_seqlens.numel() != B + 1:
+        raise ValueError(f"{where}: cu_seqlens must have num_requests + 1 elements")
+    if not 0 <= tb < te <= input_ids.numel() or rb < 0 or rc < 1 or rb + rc > B:
+        raise ValueError(f"{where}: the plan does not fit this batch (or the share is empty)")
     if shard_cu_seqlens is None:
         shard_cu_seqlens = torch.empty(max(rc, 0) + 1, dtype=torch.int32, device=dev)
     if shard_context is None:

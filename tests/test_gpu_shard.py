@@ -179,3 +179,18 @@ def test_calls_without_programmatic_launch_give_the_same_rows():
     torch.cuda.synchronize()
     for g in got:
         assert np.array_equal(g.cpu().numpy(), rows)
+
+
+def test_binding_refuses_inputs_that_do_not_fit_the_plan():
+    batch = wl.ragged_16()
+    ids, cu, ctx = dev(batch.ids), dev(batch.cu_seqlens), dev(batch.ngram_context)
+    plan = ple.ple_shard_plan(batch.cu_seqlens, batch.num_requests, batch.num_tokens, 2, 1)
+    with pytest.raises(ValueError):
+        ple.ple_shard_inputs(ids, cu[:-1], ctx, plan)          # cu_seqlens one short
+    with pytest.raises(ValueError):
+        ple.ple_shard_inputs(ids[:10], cu, ctx, plan)          # fewer ids than the plan's tokens
+    tb, te, rb, rc = plan
+    with pytest.raises(ValueError):
+        ple.ple_shard_inputs(ids, cu, ctx, (tb, te, rb, batch.num_requests))  # past the last request
+    with pytest.raises(ValueError):
+        ple.ple_shard_inputs(ids, cu, ctx, (tb, tb, rb, 0))    # an empty share
