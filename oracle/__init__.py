@@ -13,6 +13,7 @@ row-id hash into one Triton kernel", sections "What" and "Why it is safe".
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -55,26 +56,47 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """A compiled copy of ple_oracle.c at `path`, with its C signatures."""
+    lib = ctypes.CDLL(path)
+    p, i32, i64, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
+    lib.oracle_floor_mod.argtypes = [i64, i64]
+    lib.oracle_floor_mod.restype = i64
+    lib.oracle_token_index.argtypes = [p, i32, i64, c_int, p, p]
+    lib.oracle_token_index.restype = c_int
+    lib.oracle_next_context.argtypes = [p, c_int, i64, p, p, p, i32, i32, p]
+    lib.oracle_next_context.restype = c_int
+    rargs = [p, c_int, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, i64, p]
+    lib.oracle_row_embed.argtypes = rargs[:-1] + [p, i64, i32, p, p]
+    lib.oracle_row_embed.restype = c_int
+    for name in ("oracle_row_ids", "oracle_row_ids_reading_b"):
+        fn = getattr(lib, name)
+        fn.argtypes = rargs
+        fn.restype = c_int
+    return lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route this module's functions through another compiled copy of the
+    oracle (the tests' planted-mistake copies) for the duration."""
+    global _lib
+    lib = load_library(path)
+    _load()
+    with _lock:
+        saved, _lib = _lib, lib
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            p, i32, i64, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int
-            lib.oracle_floor_mod.argtypes = [i64, i64]
-            lib.oracle_floor_mod.restype = i64
-            lib.oracle_token_index.argtypes = [p, i32, i64, c_int, p, p]
-            lib.oracle_token_index.restype = c_int
-            lib.oracle_next_context.argtypes = [p, c_int, i64, p, p, p, i32, i32, p]
-            lib.oracle_next_context.restype = c_int
-            rargs = [p, c_int, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, i64, p]
-            lib.oracle_row_embed.argtypes = rargs[:-1] + [p, i64, i32, p, p]
-            lib.oracle_row_embed.restype = c_int
-            for name in ("oracle_row_ids", "oracle_row_ids_reading_b"):
-                fn = getattr(lib, name)
-                fn.argtypes = rargs
-                fn.restype = c_int
-            _lib = lib
+            _lib = load_library(build())
     return _lib
 
 

@@ -92,8 +92,11 @@ int oracle_token_index(const int32_t* cu_seqlens, int32_t num_requests, int64_t 
     }
     if (!cu_seqlens || num_requests < 1) return ORC_ERR_ARG;
     if (cu_seqlens[0] != 0 || (int64_t)cu_seqlens[num_requests] != num_tokens) return ORC_ERR_INDEX;
-    for (int32_t r = 0; r < num_requests; ++r) {
+    /* the whole layout is checked before any write, so every token written
+     * lies in [0, num_tokens) */
+    for (int32_t r = 0; r < num_requests; ++r)
         if (cu_seqlens[r + 1] < cu_seqlens[r]) return ORC_ERR_INDEX;
+    for (int32_t r = 0; r < num_requests; ++r) {
         for (int32_t t = cu_seqlens[r]; t < cu_seqlens[r + 1]; ++t) {
             req[t] = r;
             local[t] = t - cu_seqlens[r];
@@ -113,7 +116,7 @@ static int check_index(const int32_t* req, const int32_t* local, int64_t T, int3
     }
     for (int64_t t = 0; t < T; ++t) {
         int32_t r = req[t];
-        if (r < 0 || r >= B || local[t] < 0) return ORC_ERR_INDEX;
+        if (r < 0 || r >= B || local[t] < 0 || (int64_t)local[t] > t) return ORC_ERR_INDEX;
         int64_t s = t - (int64_t)local[t];
         if (start[r] < 0) start[r] = s;
         if (s != start[r] || (int64_t)local[t] != len[r]) return ORC_ERR_INDEX;
