@@ -380,6 +380,39 @@ def test_embed_of_a_one_hot_table_counts_heads_per_row(seed):
             assert np.array_equal(emb[l, t], counts.astype(np.float64))
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_embed_reads_each_layers_own_table(seed):
+    """Layer l's table holds (l + 1) * r in row r (exact in bfloat16 up to
+    256): each layer's gathered sum is (l + 1) times the sum of its row ids
+    over heads, the row ids taken from the pure-Python brute force.  A gather
+    that read another layer's table would scale the wrong sums."""
+    batch, _ = wl.small_table_batch(seed, D=2, T_max=30, L=2)
+    rng = np.random.default_rng(seed)
+    H = batch.num_heads
+    batch.vocab_sizes[:] = rng.integers(1, max(2, 127 // H), size=batch.vocab_sizes.shape)
+    batch.offsets[:] = wl.prefix_offsets(batch.vocab_sizes)
+    V = int(batch.vocab_sizes.sum(axis=1).max())
+    L = batch.num_layers
+    vals = (np.arange(L)[:, None] + 1) * np.arange(V)[None, :]
+    table = wl.bf16_bits(np.repeat(vals[:, :, None], 2, axis=2).astype(np.float32))
+    emb, _ = oracle_embed(batch, table)
+    expect = (np.arange(L)[:, None] + 1) * run_brute(batch).sum(axis=2)
+    assert np.array_equal(emb[..., 0], expect.astype(np.float64))
+    assert np.array_equal(emb[..., 1], emb[..., 0])
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_embed_abs_sum_is_the_gather_of_magnitudes(seed):
+    """The error-bound companion of the gather: the sum of |x| over the
+    gathered values equals the gather of the table with its sign bits
+    cleared."""
+    batch, table = wl.small_table_batch(seed, D=8, T_max=30)
+    _, abs_sum = oracle_embed(batch, table)
+    magnitudes, _ = oracle_embed(batch, table & np.uint16(0x7FFF))
+    assert np.array_equal(abs_sum, magnitudes)
+    assert (table & np.uint16(0x8000)).any()  # the table has negative values to clear
+
+
 def test_embed_rows_outside_the_table_add_nothing():
     batch, table = wl.small_table_batch(5, D=8, T_max=60)
     V = table.shape[1]
