@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(BUILD_DIR, "libple.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["ple_api.cu", "ple_rowids_fixed.cu", "ple_rowids_runtime.cu", "ple_rowids_small.cu", "ple_embed.cu", "ple_index.cu"]
+SOURCES = ["ple_api.cu", "ple_rowids_fixed.cu", "ple_rowids_headlane.cu", "ple_rowids_runtime.cu",
+           "ple_rowids_small.cu", "ple_embed.cu", "ple_index.cu"]
 
 
 def nvcc() -> str:

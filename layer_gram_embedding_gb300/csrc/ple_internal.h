@@ -48,6 +48,7 @@ constexpr int kFixedMinBlocks = PLE_FIXED_MIN_BLOCKS;
 constexpr int kTargetBlocksPerSm = PLE_BLOCKS_PER_SM;
 constexpr int kTargetBlocksPerSmEmbed = PLE_BLOCKS_PER_SM_EMBED;
 constexpr int kTargetBlocksPerSmI64 = PLE_BLOCKS_PER_SM_I64;
+
 // A grid with fewer blocks than this many per SM (times the SM count) takes
 // fewer warps per block, so that its warps spread over more SMs (0: never).
 #ifndef PLE_SPREAD_BLOCKS_PER_SM
@@ -158,6 +159,14 @@ cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaun
                            cudaStream_t stream);
 // The tuned (ngram_size, heads_per_ngram) pairs of the fixed-shape kernel.
 bool shape_is_fixed(int N, int hpn);
+// The shape whose heads fill a warp, with int64 row ids, is hashed by the
+// head-lane kernel (ple_rowids_headlane.cu): the choice, its shared memory,
+// tile and launch.
+bool uses_headlane_kernel(const RowIdsParams& p);
+size_t headlane_smem_bytes(int N, int warps);
+int headlane_tile_tokens();
+cudaError_t launch_row_ids_headlane(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                                    cudaStream_t stream);
 cudaError_t launch_row_ids_fixed(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                  cudaStream_t stream);
 // The small-batch kernel: whether a batch is small enough, its launch shape,

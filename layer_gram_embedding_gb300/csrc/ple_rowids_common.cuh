@@ -401,6 +401,66 @@ __device__ __forceinline__ void carry_empty_requests(const RowIdsParams& p, int 
     }
 }
 
+// A warp tile's windows: token t0 + lane's in VA and, for 64-token tiles,
+// token t0 + 32 + lane's in VB, with the carried boundary predicate.  The
+// tile's ids are fetched, each token's request is found (read from the
+// index, synthesised for a decode, or searched in cu_seqlens, per kIdx), the
+// ids are staged in shared memory at ids_s (with their N-1 halo) and the
+// windows built; with kCarry the first layer group's blocks also write the
+// next context.  Every lane of the warp calls it, with ntile > 0.
+template <typename IdT, int N, int kTile, int kIdx, bool kCarry>
+__device__ __forceinline__ void tile_windows(const RowIdsParams& p, int64_t* ids_s, int64_t t0,
+                                             int ntile, int lane, int64_t (&VA)[N],
+                                             int64_t (&VB)[N]) {
+    const int nA = min(32, ntile);
+    const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
+    // the tile's ids are fetched into registers first and stored to
+    // shared memory only after the index is found, so the ids loads and
+    // the index loads (or the cu_seqlens search) are in flight together
+    const TileIds fetched = fetch_tile_ids<IdT>(p, t0, ntile, N, lane);
+    int32_t rA, qA, rB, qB;
+    if constexpr (kIdx == kIdxCu) {
+        // the requests of the tile's first and last tokens bound every
+        // token's owner: with at most 32 requests between them the lanes
+        // rank the requests' starts (no search at all inside one
+        // request), else each lane searches between them
+        int ra, rb;
+        warp_owners(p, t0, t0 + ntile - 1, lane, ra, rb);
+        if (ra == rb) {
+            // the whole tile inside one request
+            const int64_t start = __ldg(p.cu + ra);
+            rA = lane < nA ? ra : 0;
+            rB = lane < nB ? ra : 0;
+            qA = lane < nA ? (int32_t)min(max(t0 + lane - start, (int64_t)0), t0 + lane) : 0;
+            qB = lane < nB
+                     ? (int32_t)min(max(t0 + 32 + lane - start, (int64_t)0), t0 + 32 + lane)
+                     : 0;
+        } else if (rb - ra <= 32) {
+            tile_owners(p, ra, rb, t0 + lane, lane < nA, t0 + 32 + lane, lane < nB, lane, rA,
+                        qA, rB, qB);
+        } else {
+            load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA, ra, rb);
+            load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB, ra, rb);
+        }
+    } else {
+        load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA);
+        load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB);
+    }
+    put_tile_ids<IdT>(p, fetched, ids_s, t0, ntile, N, lane);
+    window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
+    if constexpr (kTile == 64) {
+        window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
+    } else {
+#pragma unroll
+        for (int s = 0; s < N; ++s) VB[s] = 0;
+    }
+    if (kCarry && blockIdx.y == 0) {
+        carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
+        if constexpr (kTile == 64)
+            carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
+    }
+}
+
 // Hash one layer for one token into its int64 staging row (8-byte stores).
 template <int NMAX, int NT, bool kFast>
 __device__ __forceinline__ void hash_layer(const int64_t (&V)[NMAX], int N, int hpn,

@@ -16,7 +16,8 @@
 // than 16 heads stage one 32-token half (a 16-token quarter on the general
 // path) at a time, and in the cu_seqlens search mode take 32-token tiles.
 // Heads off the 32-bit fast path (vocab outside (0, 2^29]) stage int64 rows
-// and read them out 8 bytes at a time.
+// and read them out 8 bytes at a time.  The (5,8) shape with int64 row ids
+// runs the head-lane kernel instead (ple_rowids_headlane.cu).
 #include "ple_rowids_common.cuh"
 
 namespace ple {
@@ -202,53 +203,7 @@ row_ids_fixed_kernel(const RowIdsParams p) {
     const int nA = min(32, ntile);
     const int nB = ntile - 32;  // tokens in the second half (may be <= 0)
     int64_t VA[N], VB[N];
-    if (ntile > 0) {
-        // the tile's ids are fetched into registers first and stored to
-        // shared memory only after the index is found, so the ids loads and
-        // the index loads (or the cu_seqlens search) are in flight together
-        const TileIds fetched = fetch_tile_ids<IdT>(p, t0, ntile, N, lane);
-        int32_t rA, qA, rB, qB;
-        if constexpr (kIdx == kIdxCu) {
-            // the requests of the tile's first and last tokens bound every
-            // token's owner: with at most 32 requests between them the lanes
-            // rank the requests' starts (no search at all inside one
-            // request), else each lane searches between them
-            int ra, rb;
-            warp_owners(p, t0, t0 + ntile - 1, lane, ra, rb);
-            if (ra == rb) {
-                // the whole tile inside one request
-                const int64_t start = __ldg(p.cu + ra);
-                rA = lane < nA ? ra : 0;
-                rB = lane < nB ? ra : 0;
-                qA = lane < nA ? (int32_t)min(max(t0 + lane - start, (int64_t)0), t0 + lane) : 0;
-                qB = lane < nB
-                         ? (int32_t)min(max(t0 + 32 + lane - start, (int64_t)0), t0 + 32 + lane)
-                         : 0;
-            } else if (rb - ra <= 32) {
-                tile_owners(p, ra, rb, t0 + lane, lane < nA, t0 + 32 + lane, lane < nB, lane, rA,
-                            qA, rB, qB);
-            } else {
-                load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA, ra, rb);
-                load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB, ra, rb);
-            }
-        } else {
-            load_index<kIdx>(p, t0 + lane, lane < nA, rA, qA);
-            load_index<kIdx>(p, t0 + 32 + lane, lane < nB, rB, qB);
-        }
-        put_tile_ids<IdT>(p, fetched, ids_s, t0, ntile, N, lane);
-        window_at<IdT, N, N>(p, ids_s, lane, lane < nA, N, rA, qA, VA);
-        if constexpr (kTile == 64) {
-            window_at<IdT, N, N>(p, ids_s, 32 + lane, lane < nB, N, rB, qB, VB);
-        } else {
-#pragma unroll
-            for (int s = 0; s < N; ++s) VB[s] = 0;
-        }
-        if (kCarry && blockIdx.y == 0) {
-            carry_context<IdT>(p, ids_s, t0, lane, lane < nA, N, rA, qA);
-            if constexpr (kTile == 64)
-                carry_context<IdT>(p, ids_s, t0, 32 + lane, lane < nB, N, rB, qB);
-        }
-    }
+    if (ntile > 0) tile_windows<IdT, N, kTile, kIdx, kCarry>(p, ids_s, t0, ntile, lane, VA, VB);
     const bool all_fast = __syncthreads_and(fast_vote) != 0;
     if (ntile == 0) return;
 

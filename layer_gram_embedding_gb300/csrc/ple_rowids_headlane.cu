@@ -1,0 +1,144 @@
+// The PLE n-gram row-id hash on sm_103a: the head-lane kernel, for the tuned
+// shape whose heads fill a warp (ngram_size 5, 8 heads per order: 32 heads),
+// with int64 row ids.
+//
+// The fixed-shape kernel (ple_rowids_fixed.cu) keeps one token per lane all
+// the way through, so every lane reloads each head's constants from shared
+// memory, and the rows go through a staged tile to reach coalesced stores.
+// When a token's heads are exactly the warp's 32 lanes the hash can turn the
+// warp around instead:
+//   - the tile's windows are built one token per lane (the shared tile_windows
+//     of ple_rowids_common.cuh), and each lane folds its token's mixes, one per
+//     n-gram order, and stages them in shared memory (FreeToken PR #338,
+//     "perf(ple): fuse the n-gram row-id hash into one Triton kernel", section
+//     "What": the per-n-gram multiply / XOR loop);
+//   - then lane h takes head h for every token of the tile: its head's
+//     remainder constants stay in its registers for the whole layer, it reads
+//     its order's mix for each token (the lanes of one order read one word: a
+//     broadcast), and the warp stores one token's 32 row ids as one
+//     contiguous 256-byte run of [L, T, H] -- the floored remainder plus
+//     offset of section "What" / "Why it is safe".
+// No block barrier, no shared constants, no staged readout: the warps of a
+// block are independent from the start.  Every warp derives its own heads'
+// reciprocals (four times the fixed-shape kernel's divisions), which the
+// stores hide.  Measured on GB300 against the fixed-shape kernel, the
+// 48-layer mixed batch: 17.25 -> 15.62 us in one launch, 16.41 -> 15.19 us
+// reading an index, 16.84 -> 15.34 us with prepared constants (one-layer
+// groups; two- and three-layer groups were slower).
+#include "ple_rowids_common.cuh"
+
+namespace ple {
+namespace {
+
+constexpr int kHeadlaneTile = 32;
+
+// Shared memory per warp: the staged ids (kHaloSlots + kTileTokens int64, the
+// layout tile_windows expects) and the mixes, one row of N 8-byte words per
+// token (N - 1 orders and a pad word: an odd row pitch, so the lanes' 8-byte
+// stores of one order hit distinct banks, and the four words one token's
+// orders occupy are read without conflict).
+__host__ __device__ constexpr size_t headlane_warp_bytes(int N) {
+    return (size_t)(kHaloSlots + kTileTokens) * 8 + (size_t)kHeadlaneTile * N * 8;
+}
+
+template <typename IdT, int NT, int HPT, bool kCarry, int kIdx>
+__global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
+row_ids_headlane_kernel(const RowIdsParams p) {
+    constexpr int N = NT;
+    constexpr int H = (NT - 1) * HPT;
+    static_assert(H == 32, "one head per lane");
+    const int G = p.group_layers;
+    const int l0 = blockIdx.y * G;
+    const int gl = min(G, p.L - l0);
+    const int nwarps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    wait_prior_grid();
+    if constexpr (kCarry) carry_empty_requests<IdT>(p, N);
+    const int64_t t0 = ((int64_t)blockIdx.x * nwarps + warp) * kHeadlaneTile;
+    const int ntile = (int)max((int64_t)0, min((int64_t)kHeadlaneTile, p.T - t0));
+    if (ntile == 0) return;  // no block barrier follows
+    unsigned char* wbase = smem + (size_t)warp * headlane_warp_bytes(N);
+    int64_t* ids_s = reinterpret_cast<int64_t*>(wbase) + kHaloSlots;
+    uint2* mix_s = reinterpret_cast<uint2*>(wbase + (size_t)(kHaloSlots + kTileTokens) * 8);
+    int64_t VA[N], VB[N];
+    tile_windows<IdT, N, kHeadlaneTile, kIdx, kCarry>(p, ids_s, t0, ntile, lane, VA, VB);
+
+    const int order = lane / HPT;  // this lane's head h = lane is of order n = order + 2
+#pragma unroll 1
+    for (int l = 0; l < gl; ++l) {
+        const int64_t layer = (int64_t)l0 + l;
+        // this lane's head's constants, loaded (prepared) or derived, while
+        // the lane folds its token's mixes
+        const int64_t k = layer * H + lane;
+        const HeadConst c = p.heads != nullptr ? load_head_const(p.heads, k)
+                                               : make_head_const(p.vocab[k], p.offsets[k]);
+        const long long* ml = reinterpret_cast<const long long*>(p.mult) + layer * N;
+        uint64_t mix = (uint64_t)VA[0] * (uint64_t)__ldg(ml);
+#pragma unroll
+        for (int s = 1; s < N; ++s) {
+            // order n = s + 1 folds shifts 0..s; staged in offset binary
+            mix ^= (uint64_t)VA[s] * (uint64_t)__ldg(ml + s);
+            const OffsetBinary u = offset_binary(mix);
+            mix_s[lane * N + (s - 1)] = make_uint2(u.lo, u.hi);
+        }
+        __syncwarp();
+        long long* dst = static_cast<long long*>(p.out) + (layer * p.T + t0) * H + lane;
+        if (c.ext.z == kHeadFast) {
+            const uint32_t nv = (uint32_t)((int32_t)c.fast.z >> 1);  // -v
+#pragma unroll 4
+            for (int tt = 0; tt < ntile; ++tt) {
+                const uint2 w = mix_s[tt * N + order];
+                const OffsetBinary u = {w.x, w.y};
+                __stcs(dst + (int64_t)tt * H,
+                       (long long)((uint64_t)c.off + floormod_fast(u, c.fast, nv)));
+            }
+        } else {
+#pragma unroll 1
+            for (int tt = 0; tt < ntile; ++tt) {
+                const uint2 w = mix_s[tt * N + order];
+                const OffsetBinary u = {w.x, w.y};
+                __stcs(dst + (int64_t)tt * H, (long long)row_general(u, c.fast, c.off, c.ext));
+            }
+        }
+        __syncwarp();  // the next layer overwrites the staged mixes
+    }
+}
+
+template <typename IdT, bool kCarry>
+KernelFn pick_headlane(int mode) {
+    if (mode == kIdxDecode) return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxDecode>;
+    if (mode == kIdxCu) return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxCu>;
+    return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxArrays>;
+}
+
+template <typename IdT>
+KernelFn pick_headlane(bool carry, int mode) {
+    return carry ? pick_headlane<IdT, true>(mode) : pick_headlane<IdT, false>(mode);
+}
+
+}  // namespace
+
+// int64 row ids only: with int32 ones the fixed-shape kernel measured faster
+// (the 48-layer mixed batch 13.1 us against 13.8-14.7 us for the head-lane
+// kernel at any layer grouping), since every warp derives its own heads'
+// reciprocals here, and that work is not hidden behind half-size stores.
+bool uses_headlane_kernel(const RowIdsParams& p) {
+    return p.N == 5 && p.hpn == 8 && p.out_bytes == 8;
+}
+
+size_t headlane_smem_bytes(int N, int warps) { return (size_t)warps * headlane_warp_bytes(N); }
+
+int headlane_tile_tokens() { return kHeadlaneTile; }
+
+cudaError_t launch_row_ids_headlane(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
+                                    cudaStream_t stream) {
+    const bool carry = p.next_ctx != nullptr;
+    const KernelFn fn = id_bytes == 4 ? pick_headlane<int32_t>(carry, p.index_mode)
+                                      : pick_headlane<int64_t>(carry, p.index_mode);
+    return launch_fn(fn, p, cfg, stream);
+}
+
+}  // namespace ple

@@ -109,12 +109,16 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     RowIdsLaunch cfg;
     cfg.small = false;
     const bool fixed_shape = !runtime_layout && uses_fixed_kernel(p);
-    const int tile = fixed_shape ? fixed_tile_tokens(p.H) : kTileTokens;
+    const bool headlane = fixed_shape && uses_headlane_kernel(p);
+    const int tile = headlane      ? headlane_tile_tokens()
+                     : fixed_shape ? fixed_tile_tokens(p.H)
+                                   : kTileTokens;
     const int64_t tiles = (p.T + tile - 1) / tile;
     int warps = (int)(tiles < kMaxWarps ? tiles : kMaxWarps);
     p.stage_pitch = p.H | 1;
-    const size_t per_warp =
-        (size_t)(kHaloSlots + kTileTokens) * 8 + stage_bytes(p.H, fixed_shape);
+    const size_t per_warp = headlane ? headlane_smem_bytes(p.N, 1)
+                                     : (size_t)(kHaloSlots + kTileTokens) * 8 +
+                                           stage_bytes(p.H, fixed_shape);
 
     // layer groups: split the layers until there are per_sm blocks per SM,
     // so the last wave is short even when T alone gives few tiles; constants
@@ -133,7 +137,9 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     groups = (p.L + G - 1) / G;
     p.group_layers = G;
 
-    const size_t fixed = head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
+    // the head-lane kernel keeps each head's constants in its lane's registers
+    const size_t fixed =
+        headlane ? 0 : head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
     while (warps > 1 && fixed + warps * per_warp > (size_t)dev.max_smem_optin) --warps;
     // a small grid (a medium batch with few layers) spreads its warp tiles
     // over more SMs with fewer warps per block
@@ -150,6 +156,8 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
 cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                            cudaStream_t stream) {
     if (cfg.small) return launch_row_ids_small(p, id_bytes, cfg, stream);
+    if (uses_fixed_kernel(p) && uses_headlane_kernel(p))
+        return launch_row_ids_headlane(p, id_bytes, cfg, stream);
     if (uses_fixed_kernel(p)) return launch_row_ids_fixed(p, id_bytes, cfg, stream);
     KernelFn fn;
     if (p.out_bytes == 4)
