@@ -1,23 +1,25 @@
 // The PLE n-gram row-id hash on sm_103a: the head-lane kernel, for the tuned
-// shape whose heads fill a warp (ngram_size 5, 8 heads per order: 32 heads),
-// with int64 row ids.
+// shapes whose heads divide a warp evenly (ngram_size 5 with 8 heads per
+// order: 32 heads, one token a step; ngram_size 3 with 4: 8 heads, four
+// tokens a step), with int64 row ids.
 //
 // The fixed-shape kernel (ple_rowids_fixed.cu) keeps one token per lane all
 // the way through, so every lane reloads each head's constants from shared
 // memory, and the rows go through a staged tile to reach coalesced stores.
-// When a token's heads are exactly the warp's 32 lanes the hash can turn the
-// warp around instead:
+// When a token's heads divide the warp's 32 lanes the hash can turn the warp
+// around instead:
 //   - the tile's windows are built one token per lane (the shared tile_windows
 //     of ple_rowids_common.cuh), and each lane folds its token's mixes, one per
 //     n-gram order, and stages them in shared memory (FreeToken PR #338,
 //     "perf(ple): fuse the n-gram row-id hash into one Triton kernel", section
 //     "What": the per-n-gram multiply / XOR loop);
-//   - then lane h takes head h for every token of the tile: its head's
-//     remainder constants stay in its registers for the whole layer, it reads
-//     its order's mix for each token (the lanes of one order read one word: a
-//     broadcast), and the warp stores one token's 32 row ids as one
-//     contiguous 256-byte run of [L, T, H] -- the floored remainder plus
-//     offset of section "What" / "Why it is safe".
+//   - then lane l takes head l mod H for every (32 / H)-th token of the tile:
+//     its head's remainder constants stay in its registers for the whole
+//     layer, it reads its order's mix for each of its tokens (the lanes of one
+//     order and token read one word: a broadcast), and the warp stores the
+//     32 row ids of a step's tokens as one contiguous 256-byte run of
+//     [L, T, H] -- the floored remainder plus offset of section "What" /
+//     "Why it is safe".
 // No block barrier, no shared constants, no staged readout: the warps of a
 // block are independent from the start.  Every warp derives its own heads'
 // reciprocals (four times the fixed-shape kernel's divisions), which the
@@ -46,7 +48,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_headlane_kernel(const RowIdsParams p) {
     constexpr int N = NT;
     constexpr int H = (NT - 1) * HPT;
-    static_assert(H == 32, "one head per lane");
+    static_assert(32 % H == 0, "the heads divide the warp");
+    constexpr int TPS = 32 / H;  // tokens per hash step
     const int G = p.group_layers;
     const int l0 = blockIdx.y * G;
     const int gl = min(G, p.L - l0);
@@ -66,13 +69,15 @@ row_ids_headlane_kernel(const RowIdsParams p) {
     int64_t VA[N], VB[N];
     tile_windows<IdT, N, kHeadlaneTile, kIdx, kCarry>(p, ids_s, t0, ntile, lane, VA, VB);
 
-    const int order = lane / HPT;  // this lane's head h = lane is of order n = order + 2
+    const int head = lane % H;
+    const int sub = lane / H;         // which of the step's tokens
+    const int order = head / HPT;     // head h is of order n = order + 2
 #pragma unroll 1
     for (int l = 0; l < gl; ++l) {
         const int64_t layer = (int64_t)l0 + l;
         // this lane's head's constants, loaded (prepared) or derived, while
         // the lane folds its token's mixes
-        const int64_t k = layer * H + lane;
+        const int64_t k = layer * H + head;
         const HeadConst c = p.heads != nullptr ? load_head_const(p.heads, k)
                                                : make_head_const(p.vocab[k], p.offsets[k]);
         const long long* ml = reinterpret_cast<const long long*>(p.mult) + layer * N;
@@ -85,48 +90,59 @@ row_ids_headlane_kernel(const RowIdsParams p) {
             mix_s[lane * N + (s - 1)] = make_uint2(u.lo, u.hi);
         }
         __syncwarp();
-        long long* dst = static_cast<long long*>(p.out) + (layer * p.T + t0) * H + lane;
+        long long* dst = static_cast<long long*>(p.out) + (layer * p.T + t0 + sub) * H + head;
         if (c.ext.z == kHeadFast) {
             const uint32_t nv = (uint32_t)((int32_t)c.fast.z >> 1);  // -v
 #pragma unroll 4
-            for (int tt = 0; tt < ntile; ++tt) {
+            for (int tt = sub; tt < ntile; tt += TPS) {
                 const uint2 w = mix_s[tt * N + order];
                 const OffsetBinary u = {w.x, w.y};
-                __stcs(dst + (int64_t)tt * H,
+                __stcs(dst + (int64_t)(tt - sub) * H,
                        (long long)((uint64_t)c.off + floormod_fast(u, c.fast, nv)));
             }
         } else {
 #pragma unroll 1
-            for (int tt = 0; tt < ntile; ++tt) {
+            for (int tt = sub; tt < ntile; tt += TPS) {
                 const uint2 w = mix_s[tt * N + order];
                 const OffsetBinary u = {w.x, w.y};
-                __stcs(dst + (int64_t)tt * H, (long long)row_general(u, c.fast, c.off, c.ext));
+                __stcs(dst + (int64_t)(tt - sub) * H,
+                       (long long)row_general(u, c.fast, c.off, c.ext));
             }
         }
         __syncwarp();  // the next layer overwrites the staged mixes
     }
 }
 
-template <typename IdT, bool kCarry>
+template <typename IdT, int NT, int HPT, bool kCarry>
 KernelFn pick_headlane(int mode) {
-    if (mode == kIdxDecode) return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxDecode>;
-    if (mode == kIdxCu) return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxCu>;
-    return row_ids_headlane_kernel<IdT, 5, 8, kCarry, kIdxArrays>;
+    if (mode == kIdxDecode) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxDecode>;
+    if (mode == kIdxCu) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxCu>;
+    return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxArrays>;
+}
+
+template <typename IdT, int NT, int HPT>
+KernelFn pick_headlane(bool carry, int mode) {
+    return carry ? pick_headlane<IdT, NT, HPT, true>(mode) : pick_headlane<IdT, NT, HPT, false>(mode);
 }
 
 template <typename IdT>
-KernelFn pick_headlane(bool carry, int mode) {
-    return carry ? pick_headlane<IdT, true>(mode) : pick_headlane<IdT, false>(mode);
+KernelFn pick_headlane(int N, bool carry, int mode) {
+    return N == 3 ? pick_headlane<IdT, 3, 4>(carry, mode) : pick_headlane<IdT, 5, 8>(carry, mode);
 }
 
 }  // namespace
 
-// int64 row ids only: with int32 ones the fixed-shape kernel measured faster
-// (the 48-layer mixed batch 13.1 us against 13.8-14.7 us for the head-lane
-// kernel at any layer grouping), since every warp derives its own heads'
-// reciprocals here, and that work is not hidden behind half-size stores.
+// The shapes whose heads divide the warp evenly among the tuned ones, with
+// int64 row ids: 32 heads (one token a step) and 8 (four).  Measured on
+// GB300 against the fixed-shape kernel: the ragged 16-request batch (8 heads)
+// 2.90 -> 2.43 us a call.  With int32 row ids the fixed-shape kernel
+// measured faster (the 48-layer mixed batch 13.1 us against 13.7-14.7 us
+// here at any layer grouping: every warp derives its own heads' reciprocals,
+// and half-size stores do not hide that), and so did the 12-head shape,
+// where a step's 24 lanes leave 8 idle and its 192-byte stores straddle
+// cache lines (the large prefill 29.9 -> 41.9 us).
 bool uses_headlane_kernel(const RowIdsParams& p) {
-    return p.N == 5 && p.hpn == 8 && p.out_bytes == 8;
+    return p.out_bytes == 8 && ((p.N == 5 && p.hpn == 8) || (p.N == 3 && p.hpn == 4));
 }
 
 size_t headlane_smem_bytes(int N, int warps) { return (size_t)warps * headlane_warp_bytes(N); }
@@ -136,8 +152,8 @@ int headlane_tile_tokens() { return kHeadlaneTile; }
 cudaError_t launch_row_ids_headlane(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                     cudaStream_t stream) {
     const bool carry = p.next_ctx != nullptr;
-    const KernelFn fn = id_bytes == 4 ? pick_headlane<int32_t>(carry, p.index_mode)
-                                      : pick_headlane<int64_t>(carry, p.index_mode);
+    const KernelFn fn = id_bytes == 4 ? pick_headlane<int32_t>(p.N, carry, p.index_mode)
+                                      : pick_headlane<int64_t>(p.N, carry, p.index_mode);
     return launch_fn(fn, p, cfg, stream);
 }
 
