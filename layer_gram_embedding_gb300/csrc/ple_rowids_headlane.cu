@@ -1,7 +1,7 @@
 // The PLE n-gram row-id hash on sm_103a: the head-lane kernel, for the tuned
 // shapes whose heads divide a warp evenly (ngram_size 5 with 8 heads per
 // order: 32 heads, one token a step; ngram_size 3 with 4: 8 heads, four
-// tokens a step), with int64 row ids.
+// tokens a step).
 //
 // The fixed-shape kernel (ple_rowids_fixed.cu) keeps one token per lane all
 // the way through, so every lane reloads each head's constants from shared
@@ -17,16 +17,18 @@
 //     its head's remainder constants stay in its registers for the whole
 //     layer, it reads its order's mix for each of its tokens (the lanes of one
 //     order and token read one word: a broadcast), and the warp stores the
-//     32 row ids of a step's tokens as one contiguous 256-byte run of
-//     [L, T, H] -- the floored remainder plus offset of section "What" /
-//     "Why it is safe".
+//     32 row ids of a step's tokens as one contiguous run of [L, T, H]
+//     (256 bytes of int64, 128 of int32) -- the floored remainder plus
+//     offset of section "What" / "Why it is safe".
 // No block barrier, no shared constants, no staged readout: the warps of a
 // block are independent from the start.  Every warp derives its own heads'
 // reciprocals (four times the fixed-shape kernel's divisions), which the
 // stores hide.  Measured on GB300 against the fixed-shape kernel, the
 // 48-layer mixed batch: 17.25 -> 15.62 us in one launch, 16.41 -> 15.19 us
 // reading an index, 16.84 -> 15.34 us with prepared constants (one-layer
-// groups; two- and three-layer groups were slower).
+// groups; two- and three-layer groups were slower).  The fully unrolled pass
+// over a full tile keeps every offset a constant; int32 row ids gain from it
+// (13.05 -> 12.58 us on the same batch), against a loss with a counted loop.
 #include "ple_rowids_common.cuh"
 
 namespace ple {
@@ -43,7 +45,16 @@ __host__ __device__ constexpr size_t headlane_warp_bytes(int N) {
     return (size_t)(kHaloSlots + kTileTokens) * 8 + (size_t)kHeadlaneTile * N * 8;
 }
 
-template <typename IdT, int NT, int HPT, bool kCarry, int kIdx>
+// A row id stored with the streaming hint: int64, or its low 32 bits.
+template <typename OutT>
+__device__ __forceinline__ void st_row(OutT* p, int64_t v) {
+    if constexpr (sizeof(OutT) == 8)
+        __stcs(reinterpret_cast<long long*>(p), (long long)v);
+    else
+        __stcs(reinterpret_cast<int*>(p), (int)v);
+}
+
+template <typename IdT, int NT, int HPT, bool kCarry, int kIdx, typename OutT>
 __global__ void __launch_bounds__(kMaxWarps * 32, kFixedMinBlocks)
 row_ids_headlane_kernel(const RowIdsParams p) {
     constexpr int N = NT;
@@ -90,59 +101,73 @@ row_ids_headlane_kernel(const RowIdsParams p) {
             mix_s[lane * N + (s - 1)] = make_uint2(u.lo, u.hi);
         }
         __syncwarp();
-        long long* dst = static_cast<long long*>(p.out) + (layer * p.T + t0 + sub) * H + head;
+        OutT* dst = static_cast<OutT*>(p.out) + (layer * p.T + t0 + sub) * H + head;
+        const uint2* mrow = mix_s + sub * N + order;
         if (c.ext.z == kHeadFast) {
             const uint32_t nv = (uint32_t)((int32_t)c.fast.z >> 1);  // -v
-#pragma unroll 4
-            for (int tt = sub; tt < ntile; tt += TPS) {
-                const uint2 w = mix_s[tt * N + order];
-                const OffsetBinary u = {w.x, w.y};
-                __stcs(dst + (int64_t)(tt - sub) * H,
-                       (long long)((uint64_t)c.off + floormod_fast(u, c.fast, nv)));
+            if (ntile == kHeadlaneTile) {
+                // a full tile: every step's offsets are compile-time
+#pragma unroll
+                for (int i = 0; i < kHeadlaneTile / TPS; ++i) {
+                    const uint2 w = mrow[i * TPS * N];
+                    st_row<OutT>(dst + i * TPS * H,
+                           (int64_t)((uint64_t)c.off +
+                                       floormod_fast(OffsetBinary{w.x, w.y}, c.fast, nv)));
+                }
+            } else {
+#pragma unroll 1
+                for (int i = 0; sub + i * TPS < ntile; ++i) {
+                    const uint2 w = mrow[i * TPS * N];
+                    st_row<OutT>(dst + i * TPS * H,
+                           (int64_t)((uint64_t)c.off +
+                                       floormod_fast(OffsetBinary{w.x, w.y}, c.fast, nv)));
+                }
             }
         } else {
 #pragma unroll 1
-            for (int tt = sub; tt < ntile; tt += TPS) {
-                const uint2 w = mix_s[tt * N + order];
-                const OffsetBinary u = {w.x, w.y};
-                __stcs(dst + (int64_t)(tt - sub) * H,
-                       (long long)row_general(u, c.fast, c.off, c.ext));
+            for (int i = 0; sub + i * TPS < ntile; ++i) {
+                const uint2 w = mrow[i * TPS * N];
+                st_row<OutT>(dst + i * TPS * H,
+                       (int64_t)row_general(OffsetBinary{w.x, w.y}, c.fast, c.off, c.ext));
             }
         }
         __syncwarp();  // the next layer overwrites the staged mixes
     }
 }
 
-template <typename IdT, int NT, int HPT, bool kCarry>
+template <typename IdT, int NT, int HPT, bool kCarry, typename OutT>
 KernelFn pick_headlane(int mode) {
-    if (mode == kIdxDecode) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxDecode>;
-    if (mode == kIdxCu) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxCu>;
-    return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxArrays>;
+    if (mode == kIdxDecode) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxDecode, OutT>;
+    if (mode == kIdxCu) return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxCu, OutT>;
+    return row_ids_headlane_kernel<IdT, NT, HPT, kCarry, kIdxArrays, OutT>;
 }
 
-template <typename IdT, int NT, int HPT>
+template <typename IdT, int NT, int HPT, typename OutT>
 KernelFn pick_headlane(bool carry, int mode) {
-    return carry ? pick_headlane<IdT, NT, HPT, true>(mode) : pick_headlane<IdT, NT, HPT, false>(mode);
+    return carry ? pick_headlane<IdT, NT, HPT, true, OutT>(mode)
+                 : pick_headlane<IdT, NT, HPT, false, OutT>(mode);
 }
 
 template <typename IdT>
-KernelFn pick_headlane(int N, bool carry, int mode) {
-    return N == 3 ? pick_headlane<IdT, 3, 4>(carry, mode) : pick_headlane<IdT, 5, 8>(carry, mode);
+KernelFn pick_headlane(int N, int out_bytes, bool carry, int mode) {
+    if (out_bytes == 4) return pick_headlane<IdT, 5, 8, int32_t>(carry, mode);
+    return N == 3 ? pick_headlane<IdT, 3, 4, int64_t>(carry, mode)
+                  : pick_headlane<IdT, 5, 8, int64_t>(carry, mode);
 }
 
 }  // namespace
 
-// The shapes whose heads divide the warp evenly among the tuned ones, with
-// int64 row ids: 32 heads (one token a step) and 8 (four).  Measured on
-// GB300 against the fixed-shape kernel: the ragged 16-request batch (8 heads)
-// 2.90 -> 2.43 us a call.  With int32 row ids the fixed-shape kernel
-// measured faster (the 48-layer mixed batch 13.1 us against 13.7-14.7 us
-// here at any layer grouping: every warp derives its own heads' reciprocals,
-// and half-size stores do not hide that), and so did the 12-head shape,
-// where a step's 24 lanes leave 8 idle and its 192-byte stores straddle
-// cache lines (the large prefill 29.9 -> 41.9 us).
+// The tuned shapes whose heads divide the warp evenly: 32 heads (one token a
+// step), int64 or int32 row ids, and 8 heads (four tokens a step), int64 row
+// ids.  Measured on GB300 against the fixed-shape kernel: the ragged
+// 16-request batch (8 heads) 2.90 -> 2.43 us a call; the 48-layer mixed
+// batch with int32 row ids 13.05 -> 12.58 us.  The 12-head shape stays on the
+// fixed-shape kernel: with 32 row ids a pass each lane needs three heads'
+// constants and the large prefill took 27.6 us with prepared constants
+// against 22.1 (int32 row ids), 57.7 against 30.4 us with int64 ones and
+// derived constants (every warp dividing for three heads a layer).
 bool uses_headlane_kernel(const RowIdsParams& p) {
-    return p.out_bytes == 8 && ((p.N == 5 && p.hpn == 8) || (p.N == 3 && p.hpn == 4));
+    return (p.N == 5 && p.hpn == 8) || (p.N == 3 && p.hpn == 4 && p.out_bytes == 8);
 }
 
 size_t headlane_smem_bytes(int N, int warps) { return (size_t)warps * headlane_warp_bytes(N); }
@@ -152,8 +177,9 @@ int headlane_tile_tokens() { return kHeadlaneTile; }
 cudaError_t launch_row_ids_headlane(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,
                                     cudaStream_t stream) {
     const bool carry = p.next_ctx != nullptr;
-    const KernelFn fn = id_bytes == 4 ? pick_headlane<int32_t>(p.N, carry, p.index_mode)
-                                      : pick_headlane<int64_t>(p.N, carry, p.index_mode);
+    const KernelFn fn = id_bytes == 4
+                            ? pick_headlane<int32_t>(p.N, p.out_bytes, carry, p.index_mode)
+                            : pick_headlane<int64_t>(p.N, p.out_bytes, carry, p.index_mode);
     return launch_fn(fn, p, cfg, stream);
 }
 
