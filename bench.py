@@ -67,7 +67,8 @@ METRIC = "row-ids/sec and % HBM roofline at large prefill; device µs/call at de
 UNIT = "row-ids/s"
 L2_BYTES = 126 * 2 ** 20
 ROTATE = 64
-KERNEL_SOURCES = ["ple_rowids_common.cuh", "ple_rowids_fixed.cu", "ple_divmod.cuh", "ple_internal.h"]
+KERNEL_SOURCES = ["ple_rowids_common.cuh", "ple_rowids_headlane.cu", "ple_divmod.cuh",
+                  "ple_internal.h"]
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "row_ids_prefill_262144_traffic.json")
 
 
@@ -622,8 +623,8 @@ def our_arm(args):
         roofline = {
             "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-            "kernel": "ple row_ids kernel (row_ids_fixed_kernel<int64, 4, 4>, requests found "
-                      "from cu_seqlens in the kernel)",
+            "kernel": "ple row_ids kernel (row_ids_headlane_kernel<int64 ids, 4, 4, int64 rows, "
+                      "block-shared constants>, requests found from cu_seqlens in the kernel)",
             "algorithmic_bytes_per_launch": kernel_bytes,
             "kernel_ms_avg": step_ms,
             "kernel_timing": f"median over {len(regions)} timed regions of {args.steps} "

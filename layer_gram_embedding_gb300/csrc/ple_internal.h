@@ -159,10 +159,12 @@ cudaError_t launch_row_ids(const RowIdsParams& p, int id_bytes, const RowIdsLaun
                            cudaStream_t stream);
 // The tuned (ngram_size, heads_per_ngram) pairs of the fixed-shape kernel.
 bool shape_is_fixed(int N, int hpn);
-// Tuned shapes whose heads divide a warp (32 heads, and 8 with int64 row
-// ids) are hashed by the head-lane kernel (ple_rowids_headlane.cu): the
-// choice, its shared memory, tile and launch.
+// Tuned shapes hashed by the head-lane kernel (ple_rowids_headlane.cu): the
+// choice, whether its heads' constants are shared by the block (in shared
+// memory, ahead of the per-warp memory), its per-warp shared memory, tile and
+// launch.
 bool uses_headlane_kernel(const RowIdsParams& p);
+bool headlane_shared_constants(const RowIdsParams& p);
 size_t headlane_smem_bytes(int N, int warps);
 int headlane_tile_tokens();
 cudaError_t launch_row_ids_headlane(const RowIdsParams& p, int id_bytes, const RowIdsLaunch& cfg,

@@ -16,8 +16,9 @@
 // than 16 heads stage one 32-token half (a 16-token quarter on the general
 // path) at a time, and in the cu_seqlens search mode take 32-token tiles.
 // Heads off the 32-bit fast path (vocab outside (0, 2^29]) stage int64 rows
-// and read them out 8 bytes at a time.  The (5,8) shape, and (3,4) with int64
-// row ids, run the head-lane kernel instead (ple_rowids_headlane.cu).
+// and read them out 8 bytes at a time.  The (5,8) shape, and (3,4) and (4,4)
+// with int64 row ids, run the head-lane kernel instead
+// (ple_rowids_headlane.cu).
 #include "ple_rowids_common.cuh"
 
 namespace ple {

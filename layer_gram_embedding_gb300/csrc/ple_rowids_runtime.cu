@@ -137,9 +137,10 @@ RowIdsLaunch plan_row_ids(RowIdsParams& p, const DeviceFacts& dev, bool runtime_
     groups = (p.L + G - 1) / G;
     p.group_layers = G;
 
-    // the head-lane kernel keeps each head's constants in its lane's registers
-    const size_t fixed =
-        headlane ? 0 : head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
+    // a head-lane kernel with per-warp constants keeps them in registers
+    const size_t fixed = headlane && !headlane_shared_constants(p)
+                             ? 0
+                             : head_const_bytes(G * p.H) + round_up((size_t)G * p.N, 2) * 8;
     while (warps > 1 && fixed + warps * per_warp > (size_t)dev.max_smem_optin) --warps;
     // a small grid (a medium batch with few layers) spreads its warp tiles
     // over more SMs with fewer warps per block
