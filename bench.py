@@ -903,6 +903,8 @@ def all_configs(args, ple, torch, device, clocks, peaks):
                "row_ids_per_call": batch.row_ids_per_call}
         calls = 300
         for name, mode, odt, prepared, build_index, pdl in variants:
+            if args.forms and name not in args.forms:
+                continue
             outs = [torch.empty((L, T, H), dtype=odt, device=device)
                     for _ in range(2 if sets > 1 else 1)]
             fns = []
@@ -1083,6 +1085,9 @@ def main(argv=None):
     ap.add_argument("--only", nargs="+", default=None, metavar="KEY",
                     help="with --configs-only: these entries only (e.g. mixed_8192, "
                          "decode_b1, decode_b1_latency, row_embed_prefill_262144_lowrep)")
+    ap.add_argument("--forms", nargs="+", default=None, metavar="NAME",
+                    help="with --configs-only: only these call forms of each workload "
+                         "(e.g. one_launch_int32_row_ids), for profiling one launch kind")
     ap.add_argument("--embed", action="store_true",
                     help="time only the fused table gather (one JSON line)")
     ap.add_argument("--embed-workload", choices=["runs", "lowrep"], default="runs")
