@@ -146,6 +146,7 @@ ple_status check_row_args(const void* input_ids, int32_t id_dtype, int64_t num_t
     p->cu = cu_seqlens;
     p->next_ctx = nullptr;
     p->heads = heads;
+    p->ones = 0xFFFFFFFFu;
     return PLE_OK;
 }
 

@@ -99,6 +99,7 @@ struct RowIdsParams {
     const int32_t* cu;      // [B+1] cu_seqlens: kIdxCu and the context carry (NULL: none)
     void* next_ctx;         // [B, N-1] carried context out, dtype of ids (NULL: none)
     const void* heads;      // [L, H] prepared head constants (NULL: derive from vocab)
+    uint32_t ones;          // 0xFFFFFFFF, opaque to the compiler (floormod_fast_alu)
 };
 
 // The table gather fused with the hash: table [L, rows, dim] bfloat16 bits,

@@ -336,10 +336,10 @@ row_ids_fixed_kernel(const RowIdsParams p) {
                     const uint4 c1 = hf[h + 1];
                     const uint32_t n0 = (uint32_t)((int32_t)c0.z >> 1);  // -v of each head
                     const uint32_t n1 = (uint32_t)((int32_t)c1.z >> 1);
-                    rA[h] = floormod_fast(uA, c0, n0);
-                    rA[h + 1] = floormod_fast(uA, c1, n1);
-                    rB[h] = floormod_fast(uB, c0, n0);
-                    rB[h + 1] = floormod_fast(uB, c1, n1);
+                    rA[h] = floormod_fast_alu(uA, c0, n0, p.ones);
+                    rA[h + 1] = floormod_fast_alu(uA, c1, n1, p.ones);
+                    rB[h] = floormod_fast_alu(uB, c0, n0, p.ones);
+                    rB[h + 1] = floormod_fast_alu(uB, c1, n1, p.ones);
                     if (h % 4 == 2) {
                         // heads h - 2 .. h + 1 complete quad h / 4
                         const int qd = (h / 4) ^ sw;

@@ -29,7 +29,8 @@
 // Measured on GB300 against the fixed-shape kernel (interleaved A/B, µs per
 // call): the 48-layer mixed batch, per warp, 17.25 -> 15.62 in one launch,
 // 16.41 -> 15.19 reading an index, 16.84 -> 15.34 with prepared constants, and
-// its int32 variant, per block, 12.66 -> 11.00; the ragged batch (8 heads, per
+// its int32 variant, per block, 12.66 -> 11.00 (10.60 with its two plain adds
+// as ALU add-mins, floormod_fast_alu); the ragged batch (8 heads, per
 // warp) 2.90 -> 2.43; the large prefill (12 heads, per block) 30.43 -> 29.92.
 // The other combinations stay on the fixed-shape kernel (they measured slower
 // here): the large prefill's int32 variant (23.5 against 22.3) and the 8-head
@@ -109,7 +110,8 @@ __device__ __forceinline__ void hash_layers_own(const RowIdsParams& p, uint2* mi
                     const uint2 w = mrow[i * TPS * P];
                     st_row(dst + i * TPS * H,
                            (int64_t)((uint64_t)c.off +
-                                     floormod_fast(OffsetBinary{w.x, w.y}, c.fast, nv)));
+                                     floormod_fast_alu(OffsetBinary{w.x, w.y}, c.fast, nv,
+                                                       p.ones)));
                 }
             } else {
 #pragma unroll 1
@@ -162,9 +164,14 @@ __device__ __forceinline__ void hash_layers_shared(const RowIdsParams& p, const 
             for (int k = 0; k < H; ++k) {
                 const int j = k % NH, q = k / NH;
                 const uint2 w = mix_s[mbase[j] + ADV * q * P];
-                st_row(dst + 32 * k,
-                       (int64_t)((uint64_t)coff[j] +
-                                 floormod_fast(OffsetBinary{w.x, w.y}, cf[j], nv[j])));
+                // the sign-fix add, and for int32 rows the offset add too,
+                // as add-mins on the ALU (floormod_fast_alu)
+                const uint32_t r =
+                    floormod_fast_alu(OffsetBinary{w.x, w.y}, cf[j], nv[j], p.ones);
+                if constexpr (sizeof(OutT) == 4)
+                    st_row(dst + 32 * k, (int64_t)min((uint32_t)coff[j] + r, p.ones));
+                else
+                    st_row(dst + 32 * k, (int64_t)((uint64_t)coff[j] + r));
             }
         } else {
             // a partial tile, or a head of the group off the 32-bit fast path
