@@ -65,15 +65,16 @@ __device__ __forceinline__ void st_row(OutT* p, int64_t v) {
 }
 
 // One lane's token: fold its mixes for every order of one layer and stage
-// them in offset binary (order n = s + 1 folds shifts 0..s).
-template <int N, typename MulT>
+// them in offset binary (order n = s + 1 folds shifts 0..s), order s - 1 at
+// mix_s[row + (s - 1) * OS].
+template <int N, int OS = 1, typename MulT>
 __device__ __forceinline__ void stage_mixes(const int64_t (&V)[N], MulT ml, uint2* mix_s, int row) {
     uint64_t mix = (uint64_t)V[0] * (uint64_t)ml(0);
 #pragma unroll
     for (int s = 1; s < N; ++s) {
         mix ^= (uint64_t)V[s] * (uint64_t)ml(s);
         const OffsetBinary u = offset_binary(mix);
-        mix_s[row + (s - 1)] = make_uint2(u.lo, u.hi);
+        mix_s[row + (s - 1) * OS] = make_uint2(u.lo, u.hi);
     }
 }
 
@@ -147,7 +148,16 @@ __device__ __forceinline__ void hash_layers_shared(const RowIdsParams& p, const 
     for (int l = 0; l < gl; ++l) {
         const int64_t layer = (int64_t)l0 + l;
         const int64_t* ml = sm.mul + l * N;
-        stage_mixes<N>(VA, [&](int s) { return ml[s]; }, mix_s, lane * P);
+        // at 32 heads a lane hashes one head, so one order, of every token:
+        // the mixes are staged order-major (pitch 34 words, 16-byte aligned
+        // rows whose starts fall 4 banks apart) and a 16-byte load brings two
+        // consecutive tokens' mixes
+        constexpr bool kOM = H == 32;
+        constexpr int PO = kHeadlaneTile + 2;
+        if constexpr (kOM)
+            stage_mixes<N, PO>(VA, [&](int s) { return ml[s]; }, mix_s, lane);
+        else
+            stage_mixes<N>(VA, [&](int s) { return ml[s]; }, mix_s, lane * P);
         __syncwarp();
         OutT* dst = out + (layer * p.T + t0) * H + lane;
         if (all_fast && ntile == kHeadlaneTile) {
@@ -160,18 +170,37 @@ __device__ __forceinline__ void hash_layers_shared(const RowIdsParams& p, const 
                 coff[j] = sm.off[l * H + head[j]];
                 nv[j] = (uint32_t)((int32_t)cf[j].z >> 1);  // -v
             }
+            // the sign-fix add, and for int32 rows the offset add too, as
+            // add-mins on the ALU (floormod_fast_alu)
+            if constexpr (kOM) {
+                const uint4* mq = reinterpret_cast<const uint4*>(mix_s + (lane / HPT) * PO);
 #pragma unroll
-            for (int k = 0; k < H; ++k) {
-                const int j = k % NH, q = k / NH;
-                const uint2 w = mix_s[mbase[j] + ADV * q * P];
-                // the sign-fix add, and for int32 rows the offset add too,
-                // as add-mins on the ALU (floormod_fast_alu)
-                const uint32_t r =
-                    floormod_fast_alu(OffsetBinary{w.x, w.y}, cf[j], nv[j], p.ones);
-                if constexpr (sizeof(OutT) == 4)
-                    st_row(dst + 32 * k, (int64_t)min((uint32_t)coff[j] + r, p.ones));
-                else
-                    st_row(dst + 32 * k, (int64_t)((uint64_t)coff[j] + r));
+                for (int i = 0; i < kHeadlaneTile / 2; ++i) {
+                    const uint4 w = mq[i];  // tokens 2i and 2i + 1
+                    const uint32_t r0 =
+                        floormod_fast_alu(OffsetBinary{w.x, w.y}, cf[0], nv[0], p.ones);
+                    const uint32_t r1 =
+                        floormod_fast_alu(OffsetBinary{w.z, w.w}, cf[0], nv[0], p.ones);
+                    if constexpr (sizeof(OutT) == 4) {
+                        st_row(dst + 64 * i, (int64_t)min((uint32_t)coff[0] + r0, p.ones));
+                        st_row(dst + 64 * i + 32, (int64_t)min((uint32_t)coff[0] + r1, p.ones));
+                    } else {
+                        st_row(dst + 64 * i, (int64_t)((uint64_t)coff[0] + r0));
+                        st_row(dst + 64 * i + 32, (int64_t)((uint64_t)coff[0] + r1));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < H; ++k) {
+                    const int j = k % NH, q = k / NH;
+                    const uint2 w = mix_s[mbase[j] + ADV * q * P];
+                    const uint32_t r =
+                        floormod_fast_alu(OffsetBinary{w.x, w.y}, cf[j], nv[j], p.ones);
+                    if constexpr (sizeof(OutT) == 4)
+                        st_row(dst + 32 * k, (int64_t)min((uint32_t)coff[j] + r, p.ones));
+                    else
+                        st_row(dst + 32 * k, (int64_t)((uint64_t)coff[j] + r));
+                }
             }
         } else {
             // a partial tile, or a head of the group off the 32-bit fast path
@@ -181,7 +210,8 @@ __device__ __forceinline__ void hash_layers_shared(const RowIdsParams& p, const 
                 const int t = r / H + ADV * (k / NH);
                 if (t < ntile) {
                     const int i = l * H + r % H;
-                    const uint2 w = mix_s[t * P + (r % H) / HPT];
+                    const uint2 w = kOM ? mix_s[((r % H) / HPT) * PO + t]
+                                        : mix_s[t * P + (r % H) / HPT];
                     const OffsetBinary u{w.x, w.y};
                     st_row(dst + 32 * k, sm.ext[i].z == kHeadFast
                                              ? row_fast(u, sm.fast[i], sm.off[i])
