@@ -154,6 +154,8 @@ __device__ __forceinline__ void hash_layers_shared(const RowIdsParams& p, const 
         // consecutive tokens' mixes
         constexpr bool kOM = H == 32;
         constexpr int PO = kHeadlaneTile + 2;
+        static_assert(!kOM || (N - 2) * PO + kHeadlaneTile <= kHeadlaneTile * P,
+                      "order-major mixes stay within the warp's staging rows");
         if constexpr (kOM)
             stage_mixes<N, PO>(VA, [&](int s) { return ml[s]; }, mix_s, lane);
         else
